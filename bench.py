@@ -1,0 +1,535 @@
+#!/usr/bin/env python
+"""Throughput of one KV-cache compression event on GB300.
+
+A step is one full compression event of the Qwen3-8B-shaped stack (16
+sequences x 36 layers x 8 KV heads, head_dim 128, bf16, 32768 cached rows per
+slice -> budget 4096, prompt 512 and recent 128 protected, 17 geometric
+offsets): tri_score, tri_select_topk, tri_compact_kv on inputs resident in
+HBM. Metric: KV tokens (cached rows of every slice before the event) scored +
+selected + compacted per second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+
+--impl reference times the oracle (the plain fp64 CPU restatement under
+oracle/) on the host cores instead, on a bounded sample of the same workload.
+Under torchrun each rank runs its own batch on its own GPU (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens scored+selected+compacted per second"
+UNIT = "KV tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (also exercised by the gloo tests on CPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: int, world: int, max_seconds: float, steps: int) -> dict:
+    """Whole-job throughput: units processed by all ranks / slowest rank's time."""
+    total = per_rank_units * world * steps
+    return {"value": total / max_seconds, "ms_per_step": 1e3 * max_seconds / steps}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.marks = {}
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0_mark="t0", t1_mark="t1") -> dict:
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        t0, t1 = self.marks.get(t0_mark, 0), self.marks.get(t1_mark, 1e30)
+        rows = [l for (t, l) in self.lines if t0 <= t <= t1 + 0.15]
+        if len(rows) < 3:  # short timed region: fall back to every sample under load
+            rows = [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peak_gbs():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_inputs(w, n_slices: int, seed: int = 0):
+    """Slices drawn like the workload (same recipe, CPU generator), with
+    centres calibrated by the oracle from n_cal queries per query head."""
+    import numpy as np
+    import torch
+
+    import oracle as orc
+    from kv_cache_compression_tri_gb300 import synth
+
+    sw = synth.scaled(w, n_seq=1, n_layers=1, n_kv_heads=n_slices, n_cal=min(w.n_cal, 1024))
+    inp = synth.make_inputs(sw, "cpu", with_queries=not w.random)
+    k = inp.k.view(n_slices, w.n_cap, w.head_dim)
+    v = inp.v.view(n_slices, w.n_cap, w.head_dim)
+    cen = None
+    if not w.random:
+        cen = orc.calibrate(inp.q.to(torch.float64).numpy(), sw.group)
+    items = []
+    for s in range(n_slices):
+        items.append({
+            "k64": k[s].to(torch.float64).numpy(),
+            "kbytes": k[s].contiguous().view(torch.uint8).numpy().reshape(w.n_cap, -1).copy(),
+            "vbytes": v[s].contiguous().view(torch.uint8).numpy().reshape(w.n_cap, -1).copy(),
+            "centre": None if cen is None else (cen[0][s], cen[1][s], cen[2][s]),
+            "p_cur": w.n_valid - 1, "slot": s,
+        })
+    return items
+
+
+def oracle_time(w, items, threads: int):
+    """Run oracle score + select + compact (or random select + compact) on the
+    items with a thread pool (ctypes releases the GIL); returns seconds."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import oracle as orc
+
+    n, P, W, B = w.n_valid, w.n_prompt, w.n_recent, w.budget
+
+    def one(it):
+        if w.random:
+            keep = orc.rand_select(0, 0, 0, 0, it["slot"], n, P, W, B)
+        else:
+            c, m, R = it["centre"]
+            sc = np.full(n, -np.inf)
+            sc[P:n - W] = orc.score_series(it["k64"][P:n - W], c, m, R, w.offsets, it["p_cur"], w.theta,
+                                           pos=np.arange(P, n - W))
+            keep = orc.select(sc, n, P, W, B)
+        kb, vb = it["kbytes"].copy(), it["vbytes"].copy()
+        orc.compact(kb, keep)
+        orc.compact(vb, keep)
+        return int(keep[-1])
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, items))
+    return time.perf_counter() - t0
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle as the reference implementation
+# ---------------------------------------------------------------------------
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    cores = host_cores()
+    n_sample = max(1, min(args.ref_slices, w.n_slices))
+    items = oracle_sample_inputs(w, n_sample)
+    for _ in range(args.warmup):
+        oracle_time(w, items[: max(1, min(len(items), cores))], cores)
+    times = [oracle_time(w, items, cores) for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    tokens = n_sample * w.n_valid
+    value = tokens / sec
+    sample = (f"{n_sample} slices of {w.name} per step ({w.n_valid} rows each, fp64 oracle: series score, "
+              f"stable-sort select, byte-loop compaction of K and V)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w) -> dict:
+    return {
+        "workload": w.name, "n_seq": w.n_seq, "n_layers": w.n_layers, "n_kv_heads": w.n_kv_heads,
+        "head_dim": w.head_dim, "n_cap": w.n_cap, "n_valid": w.n_valid, "budget": w.budget,
+        "n_prompt": w.n_prompt, "n_recent": w.n_recent, "offsets": len(w.offsets),
+        "rope_theta": w.theta, "storage": "bf16" if w.elem_bytes == 2 else "f32",
+        "path": "tri_rand_evict + tri_compact_kv" if w.random else "tri_score + tri_select_topk + tri_compact_kv",
+        "parallelism": "one cache batch per GPU (weak scaling)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, w):
+    import numpy as np
+    import torch
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+
+    from kv_cache_compression_tri_gb300 import _build
+
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build()
+    barrier()
+    import kv_cache_compression_tri_gb300 as tri
+    from kv_cache_compression_tri_gb300 import synth
+
+    tri.load_library()
+    S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    d, e = w.head_dim, w.elem_bytes
+    inp = synth.make_inputs(w, dev)
+    centers = None
+    if not w.random:
+        centers = tri.calibrate_centers(inp.q, w.group)
+        inp.q = None
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    # first B rows of every slice are all compaction can change: keep a copy
+    k_head = inp.k[:, :, :, :B].clone()
+    v_head = inp.v[:, :, :, :B].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_valid = torch.full((S,), n, dtype=torch.int32, device=dev)
+    pos_out = torch.empty(S, w.n_cap, dtype=torch.int32, device=dev)
+    kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status)
+    scores = torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def restore():
+        inp.k[:, :, :, :B].copy_(k_head)
+        inp.v[:, :, :, :B].copy_(v_head)
+        n_valid.fill_(n)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(rec=None):
+        if w.random:
+            if rec: rec[0].record(stream)
+            tri.rand_evict(kv, 0, 0, P, W, B, keep)
+            if rec: rec[1].record(stream)
+        else:
+            if rec: rec[0].record(stream)
+            tri.score(kv, centers, w.theta, w.offsets, inp.p_cur, scores, n_prompt=P, n_recent=W)
+            if rec: rec[1].record(stream)
+            tri.select_topk(scores, kv, P, W, B, keep)
+        if rec: rec[2].record(stream)
+        tri.compact_kv(kv, keep, B)
+        if rec: rec[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+        torch.cuda.synchronize()
+        restore()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    # moved rows per event (identical every step: same inputs)
+    keep_h = keep.cpu().numpy()
+    moved = int((keep_h != np.arange(B)[None, :]).sum())
+    restore()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    recs = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    l0 = tri.launch_count()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    w0 = time.perf_counter()
+    for i in range(args.steps):
+        step(recs[i])
+        restore()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    clocks.mark("t1")
+    launches = tri.launch_count() - l0
+    time.sleep(0.3)
+    clocks.stop()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    step_ms = [recs[i][0].elapsed_time(recs[i][3]) for i in range(args.steps)]
+    k1_ms = [recs[i][0].elapsed_time(recs[i][1]) for i in range(args.steps)]
+    k2_ms = [recs[i][1].elapsed_time(recs[i][2]) for i in range(args.steps)]
+    k3_ms = [recs[i][2].elapsed_time(recs[i][3]) for i in range(args.steps)]
+    dev_sec = sum(step_ms) / 1e3
+    max_sec = max_over_ranks(dev_sec, device=dev)
+    agg = aggregate(S * n, ws, max_sec, args.steps)
+
+    # algorithmic bytes
+    cand_rows = S * (n - P - W)
+    score_bytes = 0 if w.random else cand_rows * d * e
+    compact_bytes = moved * (4 * d * e + 8)
+    step_bytes = score_bytes + compact_bytes
+    mean = lambda xs: sum(xs) / len(xs)
+    peak, peak_kind = measured_peak_gbs()
+    if w.random:
+        dom_name, dom_ms, dom_bytes = "compact_kernel", mean(k3_ms), compact_bytes
+    else:
+        dom_name, dom_ms, dom_bytes = "score_kernel", mean(k1_ms), score_bytes
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = known_traffic(w.name, dom_name)
+    result = {
+        "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(w), l2="inputs larger than L2 (K+V %.1f GB); the first %d rows of every "
+                       "slice are restored between steps (%.1f GB written, also flushes L2)" % (
+                           2 * S * w.n_cap * d * e / 1e9, B, 2 * S * B * d * e / 1e9)),
+        "gbs": step_bytes / (dev_sec / args.steps) / 1e9,
+        "hbm_frac_of_8tbs": step_bytes / (dev_sec / args.steps) / 1e9 / 8000.0,
+        "algorithmic_bytes_per_step": step_bytes,
+        "kernel_ms": {"score" if not w.random else "rand_select": round(mean(k1_ms), 4),
+                      "select": round(mean(k2_ms), 4), "compact": round(mean(k3_ms), 4)},
+        "moved_rows_per_step": moved,
+        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "bytes_per_launch": dom_bytes},
+        "clocks": clocks.summary(),
+        "gpu_launches": launches,
+        "wall_ms_per_step_incl_restore": 1e3 * (w1 - w0) / args.steps,
+    }
+    del scores
+    torch.cuda.empty_cache()
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, w, tri, synth, inp, centers, dev, stream)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args, w)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def known_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it covers the
+    current kernel (profiles/traffic.json), else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        return t.get(workload, {}).get(kernel)
+    except (OSError, ValueError):
+        return None
+
+
+def run_e2e(args, w, tri, synth, inp, centers, dev, stream):
+    """Same metric through the public API with host buffers: each step copies
+    the cache in from pinned host memory, compresses it, and reads the
+    compacted rows and keep lists back."""
+    import torch
+
+    S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    per_seq = 2 * w.n_layers * w.n_kv_heads * w.n_cap * w.head_dim * w.elem_bytes
+    try:
+        import psutil
+        avail = psutil.virtual_memory().available
+    except Exception:
+        avail = 64 << 30
+    n_seq = max(1, min(w.n_seq, int(0.3 * avail) // per_seq, args.e2e_max_seqs))
+    Se = n_seq * w.n_layers * w.n_kv_heads
+    hk = torch.empty(n_seq, w.n_layers, w.n_kv_heads, w.n_cap, w.head_dim, dtype=w.dtype, pin_memory=True)
+    hv = torch.empty_like(hk, pin_memory=True)
+    hk.copy_(inp.k[:n_seq])
+    hv.copy_(inp.v[:n_seq])
+    out_k = torch.empty(n_seq, w.n_layers, w.n_kv_heads, B, w.head_dim, dtype=w.dtype, pin_memory=True)
+    out_v = torch.empty_like(out_k, pin_memory=True)
+    out_keep = torch.empty(Se, B, dtype=torch.int32, pin_memory=True)
+    dk, dv = inp.k[:n_seq], inp.v[:n_seq]
+    n_valid = torch.full((Se,), n, dtype=torch.int32, device=dev)
+    pos_out = torch.empty(Se, w.n_cap, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = tri.KVCache(dk, dv, n_valid, None, pos_out, status)
+    scores = torch.empty(Se, w.n_cap, dtype=torch.float32, device=dev)
+    keep = torch.empty(Se, B, dtype=torch.int32, device=dev)
+    p_cur = inp.p_cur[:n_seq]
+
+    def one():
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        n_valid.fill_(n)
+        if w.random:
+            tri.rand_evict(kv, 0, 0, P, W, B, keep)
+        else:
+            tri.score(kv, centers, w.theta, w.offsets, p_cur, scores, n_prompt=P, n_recent=W)
+            tri.select_topk(scores, kv, P, W, B, keep)
+        tri.compact_kv(kv, keep, B)
+        out_k.copy_(dk[:, :, :, :B], non_blocking=True)
+        out_v.copy_(dv[:, :, :, :B], non_blocking=True)
+        out_keep.copy_(keep, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, args.e2e_steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    sec = max(e0.elapsed_time(e1) / 1e3, wall)
+    h2d = 2 * hk.numel() * hk.element_size()
+    d2h = 2 * out_k.numel() * out_k.element_size() + out_keep.numel() * 4
+    assert int(status.item()) == 0
+    res = {"value": Se * n * steps / sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": steps, "n_seq": n_seq}
+    if n_seq != w.n_seq:
+        res["note"] = f"host-buffer leg runs {n_seq} of {w.n_seq} sequences (pinned host memory bound)"
+    del hk, hv, out_k, out_v
+    return res
+
+
+def cpu_baseline(args, w):
+    cores = host_cores()
+    items = oracle_sample_inputs(w, args.cpu_slices)
+    oracle_time(w, items[:1], 1)  # warm the library
+    sec = oracle_time(w, items, cores)
+    tokens = len(items) * w.n_valid
+    return {"value": tokens / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(items)} slices drawn like {w.name} ({w.n_valid} rows each), fp64 oracle "
+                      f"score/select/compact, {cores} threads, {sec:.1f} s"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gpu", "reference", "ours"], default="gpu")
+    ap.add_argument("--workload", default="qwen3_8b_stack")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-max-seqs", type=int, default=16)
+    ap.add_argument("--cpu-slices", type=int, default=32)
+    ap.add_argument("--ref-slices", type=int, default=16)
+    args = ap.parse_args(argv)
+    from kv_cache_compression_tri_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

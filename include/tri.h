@@ -1,0 +1,213 @@
+/*
+ * tri.h -- C ABI of the GB300 KV-cache compression library (libtri.so).
+ *
+ * The library scores every cached key of every KV head with the TriAttention
+ * trigonometric series, keeps a per-head budget of keys under a protected
+ * prompt prefix and recent window, compacts K/V in place, and offers the
+ * Random Attention variant that keeps a uniform random subset instead of
+ * scoring. Every call is asynchronous on the caller's CUDA stream.
+ *
+ * Sources, cited by page title and section / equation:
+ *   [TA] "TriAttention: Efficient Long Reasoning with Trigonometric KV
+ *        Compression" (paper summary page), section 3.4.
+ *   [TB] the TriAttention blog page (same title), "TriAttention Scoring",
+ *        code-level implementation and S_norm paragraphs, "actual flow".
+ *   [RA] "Random Attention: Rethinking KV Cache Eviction for Efficient
+ *        Reasoning", section 2 (Eq. 2), section 3 (Eq. 3, Algorithm 1),
+ *        Appendix F (engine details).
+ *
+ * Conventions for every entry point
+ *   - A "slice" is one (sequence, layer, KV head) row block of the cache;
+ *     slice s = (seq * n_layers + layer) * n_kv_heads + head.
+ *   - Pointers documented as "device" must be device (or managed) memory
+ *     owned by the caller; the library never allocates, frees or retains
+ *     caller memory and keeps no per-call state (calls are thread-safe).
+ *   - Scratch memory, where an entry point needs it, is passed in by the
+ *     caller with its size from the matching *_workspace_bytes() query.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and return TRI_ERR_INVALID_ARG / TRI_ERR_UNSUPPORTED; nothing is
+ *     launched in that case. TRI_ERR_CUDA means a launch failed (the CUDA
+ *     error is left for the caller's cudaGetLastError()).
+ *   - Input faults only visible on the device (n_valid > n_cap, a NaN score,
+ *     a malformed keep list) are reported through the caller's optional
+ *     device word *dev_status (first error wins, TRI_DEV_* codes); kernels
+ *     never trap. A slice with a fault is skipped by the kernel that found
+ *     it.
+ */
+#ifndef TRI_H_
+#define TRI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA stream handle, the same type as cudaStream_t (NULL = the legacy
+ * default stream). */
+typedef struct CUstream_st* tri_stream_t;
+
+typedef enum {
+  TRI_OK = 0,
+  TRI_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or budget    */
+  TRI_ERR_UNSUPPORTED = 2, /* head_dim, dtype or device not supported          */
+  TRI_ERR_CUDA = 3,        /* a kernel launch failed                           */
+  TRI_ERR_TIMEOUT = 4      /* reserved: no entry point waits on anything today */
+} tri_status;
+
+/* Device status word values (written with atomicCAS from 0, first error wins). */
+#define TRI_DEV_OK 0
+#define TRI_DEV_NVALID_OVER_CAP 1 /* n_valid[s] > n_cap: slice skipped            */
+#define TRI_DEV_NAN_SCORE 2       /* a candidate score was NaN (ranked lowest)    */
+#define TRI_DEV_BAD_KEEP 3        /* keep list not ascending / out of range       */
+
+typedef enum { TRI_F32 = 0, TRI_BF16 = 1 } tri_dtype;
+
+/* How band f pairs two coordinates of a head vector into one complex number:
+ * interleaved (x[2f], x[2f+1]) as [TA] "RoPE in complex form" writes it, or
+ * half-split (x[f], x[f+d/2]) -- the other rotation style [TB]'s invert_rope
+ * call accepts. Both the query statistics and the keys use the same style. */
+typedef enum { TRI_ROPE_INTERLEAVED = 0, TRI_ROPE_HALF = 1 } tri_rope_style;
+
+/* Norm term: weighted S_norm = sum_f (1 - R_f) E|q_f| |k_f| ([TA] "Adaptive
+ * Weighting via Q/K Concentration"), or the unweighted ablation
+ * S_norm^(0) = sum_f E|q_f| |k_f| ([TA] "The Norm-Based Term"). */
+typedef enum { TRI_NORM_WEIGHTED = 0, TRI_NORM_UNWEIGHTED = 1 } tri_norm_mode;
+
+/* The cache. K and V rows are head_dim elements, contiguous; slice s starts
+ * at element s * slice_stride of k (and of v); row i of the slice at element
+ * s * slice_stride + i * head_dim. k and v: device, 16-byte aligned,
+ * slice_stride * element size a multiple of 16 bytes. */
+typedef struct {
+  void* k;               /* [n_slices][n_cap][head_dim] pre-RoPE keys            */
+  void* v;               /* [n_slices][n_cap][head_dim] values                   */
+  int32_t* pos;          /* device [n_slices][n_cap] token positions, or NULL:
+                            NULL means position = slot index (a fresh cache)    */
+  int32_t* pos_out;      /* device [n_slices][n_cap]: where compaction writes the
+                            survivors' positions; may equal pos                 */
+  int32_t* n_valid;      /* device [n_slices]: cached rows per slice; compaction
+                            sets it to the number kept                          */
+  int64_t slice_stride;  /* elements between slices, >= n_cap * head_dim        */
+  int32_t n_seq, n_layers, n_kv_heads;
+  int32_t n_cap;         /* row capacity of a slice                              */
+  int32_t head_dim;      /* 64 or 128                                            */
+  tri_dtype dtype;       /* element type of k and v                              */
+  int32_t* dev_status;   /* device int32 status word (TRI_DEV_*), or NULL        */
+} tri_kv;
+
+/* Per-(layer, KV head) query statistics, [TA] "Offline Calibration
+ * Procedure"; index lh = layer * n_kv_heads + head, F = head_dim / 2. */
+typedef struct {
+  float* center;    /* device [n_layers * n_kv_heads][F][2]: E[q_f] (re, im)       */
+  float* mean_norm; /* device [n_layers * n_kv_heads][F]:    E|q_f|                */
+  float* mrl;       /* device [n_layers * n_kv_heads][F]:    R_f = |E q_f| / E|q_f|*/
+} tri_centers;
+
+/* ------------------------------------------------------------------------ */
+const char* tri_status_string(tri_status s); /* static text, never NULL */
+int32_t tri_abi_version(void);               /* 1 */
+/* Kernels this library has launched in this process (all devices, all
+ * threads); used to count launches inside a timed region. */
+uint64_t tri_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * tri_calibrate_centers -- offline per-head query statistics.
+ * [TA] "Offline Calibration Procedure" and "Measurement via Mean Resultant
+ * Length": for each layer, KV head h and band f, pooling the `group` query
+ * heads h*group .. h*group+group-1 that share KV head h (the reading chosen
+ * for GQA: one centre per KV head, as [TB] shapes the norm coefficient
+ * [num_kv_heads, freq_count]):
+ *   center = mean of q_f (complex), mean_norm = mean of |q_f|,
+ *   mrl = |center| / mean_norm (0 when mean_norm is 0).
+ * q: device [n_layers][n_q_heads][n_tok][head_dim] pre-RoPE queries of type
+ * dtype, 16-byte aligned. n_q_heads must be a multiple of group. Sums are in
+ * fp32 with a fixed-order two-level reduction (deterministic).
+ * ws: device scratch of at least tri_calibrate_workspace_bytes(...) bytes,
+ * 16-byte aligned (may be NULL when that size is 0).
+ * ------------------------------------------------------------------------ */
+size_t tri_calibrate_workspace_bytes(int32_t n_layers, int32_t n_q_heads, int32_t group,
+                                     int32_t head_dim, int64_t n_tok);
+tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layers,
+                                 int32_t n_q_heads, int32_t group, int32_t head_dim,
+                                 int64_t n_tok, tri_rope_style style, tri_centers out,
+                                 void* ws, size_t ws_bytes, tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tri_score -- offset-averaged TriAttention score of cached keys.
+ * For every row i of slice s with n_prompt <= i < n_valid[s] - n_recent
+ * (protected rows are not scored and their score entries are left as they
+ * were), with p_i its position, age = p_cur[seq] - p_i, and the statistics of
+ * the slice's (layer, KV head):
+ *   S~(i) = (1/|D|) sum_{delta in D} sum_f |c_f||k_f| cos(w_f (age+delta) + arg c_f - arg k_f)
+ *         + sum_f wgt_f E|q_f| |k_f|
+ * [TA] "The Trigonometric Series Term" (S_trig), "Adaptive Weighting via Q/K
+ * Concentration" (S_norm, wgt_f = 1 - R_f; wgt_f = 1 under
+ * TRI_NORM_UNWEIGHTED), "The combined score", "Handling Multiple Future
+ * Positions" (average over the future offsets D); w_f = rope_theta^(-2f/d).
+ * Computed as the per-band complex multiply-accumulate
+ *   Re sum_f (c_f G_f e^{i w_f age}) conj(k_f) + norm term,
+ *   G_f = (1/|D|) sum_delta e^{i w_f delta},
+ * which is the same quantity ([TB] "implementation in code": the query-side
+ * phase carries the distance).
+ * offsets: HOST array of n_offsets (1..64) token offsets (D).
+ * p_cur: device [n_seq] int64, position of the newest cached token of each
+ * sequence (the current query position). scores: device [n_slices][n_cap]
+ * fp32. Arithmetic: fp32 FMA; phases in 64-bit fixed-point turns.
+ * ------------------------------------------------------------------------ */
+tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
+                     tri_rope_style style, tri_norm_mode norm_mode, const int32_t* offsets,
+                     int32_t n_offsets, const int64_t* p_cur, int32_t n_prompt,
+                     int32_t n_recent, float* scores, tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tri_select_topk -- per-slice budgeted selection.
+ * If n_valid[s] <= budget nothing is evicted: keep = 0 .. n_valid-1, then -1.
+ * Otherwise keep = [0, n_prompt) U top-(budget - n_prompt - n_recent) of the
+ * candidates [n_prompt, n_valid - n_recent) by score U [n_valid - n_recent,
+ * n_valid), in ascending slot order ([TA] "Retention and eviction"; [RA]
+ * Eq. 2 and section 2's never-scored recent buffer; [TB] "actual flow": the
+ * prompt is protected; [RA] Appendix F: keep-sets sorted chronologically).
+ * Equal scores keep the lower slot; -0 equals +0; NaN ranks lowest and sets
+ * TRI_DEV_NAN_SCORE. budget counts every survivor, protected rows included;
+ * requires budget >= n_prompt + n_recent.
+ * scores: device [n_slices][n_cap]; keep_idx: device [n_slices][budget].
+ * ------------------------------------------------------------------------ */
+tri_status tri_select_topk(const float* scores, const tri_kv* kv, int32_t n_prompt,
+                           int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                           tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tri_compact_kv -- in-place, order-preserving compaction.
+ * For each slice, with n_keep = the number of leading non-negative entries of
+ * keep_idx[s] (ascending, keep_idx[s][j] >= j, < n_cap): for j < n_keep, row
+ * j of K and V <- row keep_idx[s][j] (as if done for j ascending, one row at
+ * a time); pos_out[s][j] <- pos[s][keep[j]] (or keep[j] when pos is NULL);
+ * n_valid[s] <- n_keep. [RA] Appendix F: KV tensors compacted with a gather.
+ * Rows >= n_keep keep their old bytes. A malformed keep list sets
+ * TRI_DEV_BAD_KEEP and leaves that slice untouched. kv->pos_out required.
+ * ------------------------------------------------------------------------ */
+tri_status tri_compact_kv(const tri_kv* kv, const int32_t* keep_idx, int32_t budget,
+                          tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * rand_evict -- Random Attention keep lists (no score is computed).
+ * [RA] section 3, Eq. 3 and Algorithm 1: prompt rows score +inf (kept), every
+ * other candidate draws an i.i.d. uniform u_i, independently per KV head and
+ * per eviction; keep the top (budget - n_prompt - n_recent) by (u desc, slot
+ * asc); the recent buffer is kept unscored ([RA] section 2). u_i is word
+ * (i mod 4) of Philox-4x32-10 (Salmon et al., SC'11) with
+ *   counter = (i / 4, head + 65536 * layer, seq, round),
+ *   key     = (low 32 bits of seed, high 32 bits of seed).
+ * Output layout and the n_valid <= budget case as tri_select_topk.
+ * n_layers must be <= 65535 and n_kv_heads <= 65536.
+ * ------------------------------------------------------------------------ */
+tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n_prompt,
+                      int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                      tri_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRI_H_ */

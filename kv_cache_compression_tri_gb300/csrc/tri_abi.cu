@@ -1,0 +1,260 @@
+// tri_abi.cu -- the extern "C" entry points of libtri (include/tri.h).
+//
+// Each entry point validates its arguments on the host, fills a kernel
+// parameter block, and enqueues its kernels on the caller's stream. Nothing
+// here allocates device memory or synchronises. The only host arithmetic is
+// the per-band constant table of tri_score (at most 64 bands x 5 numbers,
+// from rope_theta and the offset set), computed in fp64.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "tri_internal.cuh"
+
+namespace tri {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_bytes(tri_dtype dt) { return dt == TRI_BF16 ? 2 : 4; }
+
+// Shape checks shared by every call that takes a tri_kv.
+tri_status check_kv(const tri_kv* kv, bool need_v) {
+  if (!kv) return TRI_ERR_INVALID_ARG;
+  if (kv->dtype != TRI_BF16 && kv->dtype != TRI_F32) return TRI_ERR_UNSUPPORTED;
+  if (kv->head_dim != 64 && kv->head_dim != 128) return TRI_ERR_UNSUPPORTED;
+  if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1)
+    return TRI_ERR_INVALID_ARG;
+  const int64_t n_slices = static_cast<int64_t>(kv->n_seq) * kv->n_layers * kv->n_kv_heads;
+  if (n_slices > 0x7fffffff) return TRI_ERR_INVALID_ARG;
+  if (!kv->n_valid || !aligned(kv->n_valid, 4)) return TRI_ERR_INVALID_ARG;
+  if (!kv->k || !aligned(kv->k, 16)) return TRI_ERR_INVALID_ARG;
+  if (need_v && (!kv->v || !aligned(kv->v, 16))) return TRI_ERR_INVALID_ARG;
+  if (kv->slice_stride < static_cast<int64_t>(kv->n_cap) * kv->head_dim) return TRI_ERR_INVALID_ARG;
+  if ((kv->slice_stride * elem_bytes(kv->dtype)) % 16 != 0) return TRI_ERR_INVALID_ARG;
+  if (kv->pos && !aligned(kv->pos, 4)) return TRI_ERR_INVALID_ARG;
+  if (kv->pos_out && !aligned(kv->pos_out, 4)) return TRI_ERR_INVALID_ARG;
+  if (kv->dev_status && !aligned(kv->dev_status, 4)) return TRI_ERR_INVALID_ARG;
+  return TRI_OK;
+}
+
+int64_t slices_of(const tri_kv* kv) {
+  return static_cast<int64_t>(kv->n_seq) * kv->n_layers * kv->n_kv_heads;
+}
+
+tri_status check_protect(int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t n_cap) {
+  if (n_prompt < 0 || n_recent < 0 || budget < 1) return TRI_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_prompt) + n_recent > budget) return TRI_ERR_INVALID_ARG;
+  if (budget > n_cap) return TRI_ERR_INVALID_ARG;
+  return TRI_OK;
+}
+
+// 0.64 fixed-point turns per position of band f: omega_f / (2 pi).
+uint64_t nu_fixed(double omega) {
+  const double turns = omega / (2.0 * M_PI);  // < 0.16
+  return static_cast<uint64_t>(std::ldexp(turns, 64));
+}
+
+}  // namespace
+}  // namespace tri
+
+using namespace tri;
+
+extern "C" {
+
+const char* tri_status_string(tri_status s) {
+  switch (s) {
+    case TRI_OK: return "ok";
+    case TRI_ERR_INVALID_ARG: return "invalid argument";
+    case TRI_ERR_UNSUPPORTED: return "unsupported head_dim, dtype or device";
+    case TRI_ERR_CUDA: return "CUDA launch failed";
+    case TRI_ERR_TIMEOUT: return "timed out";
+  }
+  return "unknown status";
+}
+
+int32_t tri_abi_version(void) { return 1; }
+
+uint64_t tri_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t tri_calibrate_workspace_bytes(int32_t n_layers, int32_t n_q_heads, int32_t group,
+                                     int32_t head_dim, int64_t n_tok) {
+  if (n_layers < 1 || n_q_heads < 1 || group < 1 || n_q_heads % group || head_dim < 2 || n_tok < 1)
+    return 0;
+  const int lh = n_layers * (n_q_heads / group);
+  const int sp = calibrate_split_count(lh, static_cast<int64_t>(group) * n_tok);
+  return static_cast<size_t>(lh) * sp * (head_dim / 2) * 3 * sizeof(float);
+}
+
+tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layers,
+                                 int32_t n_q_heads, int32_t group, int32_t head_dim,
+                                 int64_t n_tok, tri_rope_style style, tri_centers out,
+                                 void* ws, size_t ws_bytes, tri_stream_t stream) {
+  if (dtype != TRI_BF16 && dtype != TRI_F32) return TRI_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return TRI_ERR_UNSUPPORTED;
+  if (style != TRI_ROPE_INTERLEAVED && style != TRI_ROPE_HALF) return TRI_ERR_INVALID_ARG;
+  if (!q || !aligned(q, 16) || n_layers < 1 || n_q_heads < 1 || group < 1 ||
+      n_q_heads % group != 0 || n_tok < 1)
+    return TRI_ERR_INVALID_ARG;
+  if (!out.center || !out.mean_norm || !out.mrl || !aligned(out.center, 8) ||
+      !aligned(out.mean_norm, 4) || !aligned(out.mrl, 4))
+    return TRI_ERR_INVALID_ARG;
+  const size_t need = tri_calibrate_workspace_bytes(n_layers, n_q_heads, group, head_dim, n_tok);
+  if (ws_bytes < need || (need > 0 && (!ws || !aligned(ws, 16)))) return TRI_ERR_INVALID_ARG;
+  CalibParams p{};
+  p.q = q;
+  p.ws = static_cast<float*>(ws);
+  p.center = out.center;
+  p.mean_norm = out.mean_norm;
+  p.mrl = out.mrl;
+  p.n_q_heads = n_q_heads;
+  p.group = group;
+  p.kv_heads = n_q_heads / group;
+  p.n_tok = n_tok;
+  const int lh = n_layers * p.kv_heads;
+  p.n_split = calibrate_split_count(lh, static_cast<int64_t>(group) * n_tok);
+  const cudaError_t e = launch_calibrate(p, dtype, head_dim, style, lh, stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
+                     tri_rope_style style, tri_norm_mode norm_mode, const int32_t* offsets,
+                     int32_t n_offsets, const int64_t* p_cur, int32_t n_prompt,
+                     int32_t n_recent, float* scores, tri_stream_t stream) {
+  tri_status st = check_kv(kv, false);
+  if (st != TRI_OK) return st;
+  if (!c || !c->center || !c->mean_norm || !c->mrl || !aligned(c->center, 8)) return TRI_ERR_INVALID_ARG;
+  if (style != TRI_ROPE_INTERLEAVED && style != TRI_ROPE_HALF) return TRI_ERR_INVALID_ARG;
+  if (norm_mode != TRI_NORM_WEIGHTED && norm_mode != TRI_NORM_UNWEIGHTED) return TRI_ERR_INVALID_ARG;
+  if (!(rope_theta > 1.0) || !std::isfinite(rope_theta)) return TRI_ERR_INVALID_ARG;
+  if (!offsets || n_offsets < 1 || n_offsets > 64) return TRI_ERR_INVALID_ARG;
+  if (!p_cur || !aligned(p_cur, 8) || !scores || !aligned(scores, 4)) return TRI_ERR_INVALID_ARG;
+  if (n_prompt < 0 || n_recent < 0) return TRI_ERR_INVALID_ARG;
+
+  ScoreParams p{};
+  const int D = kv->head_dim, F = D / 2;
+  const int kpw = score_keys_per_warp_step(kv->dtype, D);
+  for (int f = 0; f < F; ++f) {
+    const double omega = std::pow(rope_theta, -2.0 * f / D);
+    p.nu[f] = nu_fixed(omega);
+    double gr = 0.0, gi = 0.0;
+    for (int j = 0; j < n_offsets; ++j) {
+      gr += std::cos(omega * offsets[j]);
+      gi += std::sin(omega * offsets[j]);
+    }
+    p.g_re[f] = static_cast<float>(gr / n_offsets);
+    p.g_im[f] = static_cast<float>(gi / n_offsets);
+    p.step_re[f] = static_cast<float>(std::cos(omega * kpw));
+    p.step_im[f] = static_cast<float>(-std::sin(omega * kpw));
+  }
+  p.k = kv->k;
+  p.pos = kv->pos;
+  p.n_valid = kv->n_valid;
+  p.p_cur = p_cur;
+  p.center = c->center;
+  p.mean_norm = c->mean_norm;
+  p.mrl = c->mrl;
+  p.scores = scores;
+  p.dev_status = kv->dev_status;
+  p.slice_stride = kv->slice_stride;
+  p.n_cap = kv->n_cap;
+  p.lh_count = kv->n_layers * kv->n_kv_heads;
+  p.n_prompt = n_prompt;
+  p.n_recent = n_recent;
+  p.norm_mode = norm_mode;
+  // ~512 KB of keys per CTA: 8 warps x rows_per_warp rows (a multiple of the
+  // warp's 8-key batch).
+  const int row_bytes = D * elem_bytes(kv->dtype);
+  int rpw = (512 * 1024 / row_bytes) / 8;
+  const int batch = 8 * kpw;
+  rpw = ((rpw + batch - 1) / batch) * batch;
+  const int cap_rpw = ((kv->n_cap + 7) / 8 + batch - 1) / batch * batch;  // small caches
+  if (cap_rpw < rpw) rpw = cap_rpw;
+  p.rows_per_warp = rpw;
+  p.tiles_per_slice = static_cast<int32_t>((kv->n_cap + 8LL * rpw - 1) / (8LL * rpw));
+  const int64_t grid = slices_of(kv) * p.tiles_per_slice;
+  if (grid > 0x7fffffff) return TRI_ERR_INVALID_ARG;
+  const cudaError_t e = launch_score(p, kv->dtype, D, style, kv->pos != nullptr,
+                                     static_cast<int>(slices_of(kv)), stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status tri_select_topk(const float* scores, const tri_kv* kv, int32_t n_prompt,
+                           int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                           tri_stream_t stream) {
+  if (!kv) return TRI_ERR_INVALID_ARG;
+  if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
+  if (!kv->n_valid || !aligned(kv->n_valid, 4)) return TRI_ERR_INVALID_ARG;
+  if (!scores || !aligned(scores, 4) || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
+  tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
+  if (slices_of(kv) > 0x7fffffff) return TRI_ERR_INVALID_ARG;
+  SelectParams p{};
+  p.scores = scores;
+  p.n_valid = kv->n_valid;
+  p.keep = keep_idx;
+  p.dev_status = kv->dev_status;
+  p.n_cap = kv->n_cap;
+  p.n_prompt = n_prompt;
+  p.n_recent = n_recent;
+  p.budget = budget;
+  p.n_layers = kv->n_layers;
+  p.n_kv_heads = kv->n_kv_heads;
+  const cudaError_t e = launch_select(p, false, static_cast<int>(slices_of(kv)), stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n_prompt,
+                      int32_t n_recent, int32_t budget, int32_t* keep_idx, tri_stream_t stream) {
+  if (!kv) return TRI_ERR_INVALID_ARG;
+  if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
+  if (kv->n_layers > 65535 || kv->n_kv_heads > 65536) return TRI_ERR_INVALID_ARG;
+  if (!kv->n_valid || !aligned(kv->n_valid, 4) || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
+  tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
+  if (slices_of(kv) > 0x7fffffff) return TRI_ERR_INVALID_ARG;
+  SelectParams p{};
+  p.n_valid = kv->n_valid;
+  p.keep = keep_idx;
+  p.dev_status = kv->dev_status;
+  p.n_cap = kv->n_cap;
+  p.n_prompt = n_prompt;
+  p.n_recent = n_recent;
+  p.budget = budget;
+  p.n_layers = kv->n_layers;
+  p.n_kv_heads = kv->n_kv_heads;
+  p.seed = seed;
+  p.round = round;
+  const cudaError_t e = launch_select(p, true, static_cast<int>(slices_of(kv)), stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status tri_compact_kv(const tri_kv* kv, const int32_t* keep_idx, int32_t budget,
+                          tri_stream_t stream) {
+  tri_status st = check_kv(kv, true);
+  if (st != TRI_OK) return st;
+  if (!kv->pos_out) return TRI_ERR_INVALID_ARG;
+  if (!keep_idx || !aligned(keep_idx, 4) || budget < 1 || budget > kv->n_cap) return TRI_ERR_INVALID_ARG;
+  CompactParams p{};
+  p.k = static_cast<char*>(kv->k);
+  p.v = static_cast<char*>(kv->v);
+  p.pos = kv->pos;
+  p.pos_out = kv->pos_out;
+  p.n_valid = kv->n_valid;
+  p.keep = keep_idx;
+  p.dev_status = kv->dev_status;
+  p.slice_bytes = kv->slice_stride * elem_bytes(kv->dtype);
+  p.n_cap = kv->n_cap;
+  p.budget = budget;
+  p.row_bytes = kv->head_dim * elem_bytes(kv->dtype);
+  const cudaError_t e = launch_compact(p, static_cast<int>(slices_of(kv)), stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+}  // extern "C"

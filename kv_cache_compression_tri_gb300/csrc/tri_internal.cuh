@@ -1,0 +1,157 @@
+// tri_internal.cuh -- device helpers and launcher declarations shared by the
+// kernels of libtri (GPU side only; the oracle has its own code).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tri.h"
+
+namespace tri {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+constexpr int MAX_BANDS = 64;  // head_dim <= 128
+
+// Count of kernels launched by the library (tri_launch_count).
+void note_launch();
+
+// First error wins: a device status word goes from 0 to `code` once.
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// bf16 halves of a 32-bit word as fp32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// e^{i 2 pi frac(x * nu)} where nu is a 0.64 fixed-point number of turns per
+// position: the product is exact mod 2^64, so the phase keeps full precision
+// at any position. Accurate variant (sincospif), for anchors.
+__device__ __forceinline__ float2 turns_rotation_accurate(int64_t x, uint64_t nu) {
+  const uint64_t t = static_cast<uint64_t>(x) * nu;  // wraps mod 2^64
+  // signed turns in [-0.5, 0.5) -> argument of sincospi in [-1, 1)
+  const float a = static_cast<float>(static_cast<int64_t>(t)) * 1.0842021724855044e-19f;  // 2^-63
+  float s, c;
+  sincospif(a, &s, &c);
+  return make_float2(c, s);
+}
+
+// Fast variant (hardware sin/cos on an argument already reduced to
+// [-pi, pi)), for per-key rotations.
+__device__ __forceinline__ float2 turns_rotation_fast(int64_t x, uint64_t nu) {
+  const uint64_t t = static_cast<uint64_t>(x) * nu;
+  const int32_t hi = static_cast<int32_t>(t >> 32);
+  const float ang = static_cast<float>(hi) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+  float s, c;
+  __sincosf(ang, &s, &c);
+  return make_float2(c, s);
+}
+
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+  return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+}
+
+// Philox-4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11): per round
+// two 32x32->64 multiplies feed the next (x0..x3); the key is bumped by the
+// Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint2 key) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      key.x += 0x9E3779B9u;
+      key.y += 0xBB67AE85u;
+    }
+    const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
+    const uint32_t hi0 = __umulhi(m0, x.x), lo0 = m0 * x.x;
+    const uint32_t hi1 = __umulhi(m1, x.z), lo1 = m1 * x.z;
+    x = make_uint4(hi1 ^ x.y ^ key.x, lo1, hi0 ^ x.w ^ key.y, lo0);
+  }
+  return x;
+}
+
+// Order-preserving map of an fp32 score to u32 (larger score -> larger key).
+// -0 is folded onto +0; NaN maps to 0 (below every number) and is flagged.
+__device__ __forceinline__ uint32_t score_key(float x, bool& nan) {
+  if (x != x) {
+    nan = true;
+    return 0u;
+  }
+  uint32_t u = __float_as_uint(x);
+  if (x == 0.0f) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel parameter blocks (passed by value).
+// ---------------------------------------------------------------------------
+struct ScoreParams {
+  const void* k;
+  const int32_t* pos;
+  const int32_t* n_valid;
+  const int64_t* p_cur;
+  const float* center;
+  const float* mean_norm;
+  const float* mrl;
+  float* scores;
+  int32_t* dev_status;
+  int64_t slice_stride;  // elements
+  int32_t n_cap;
+  int32_t lh_count;  // n_layers * n_kv_heads
+  int32_t n_prompt, n_recent;
+  int32_t norm_mode;
+  int32_t tiles_per_slice;
+  int32_t rows_per_warp;
+  uint64_t nu[MAX_BANDS];     // omega_f / 2pi as 0.64 fixed point (turns per position)
+  float g_re[MAX_BANDS];      // G_f = (1/|D|) sum_delta e^{i omega_f delta}
+  float g_im[MAX_BANDS];
+  float step_re[MAX_BANDS];   // e^{-i omega_f * (keys per warp step)}
+  float step_im[MAX_BANDS];
+};
+
+struct SelectParams {
+  const float* scores;  // [S][n_cap] (score source)
+  const int32_t* n_valid;
+  int32_t* keep;  // [S][budget]
+  int32_t* dev_status;
+  int32_t n_cap, n_prompt, n_recent, budget;
+  int32_t n_layers, n_kv_heads;
+  uint64_t seed;
+  uint32_t round;
+};
+
+struct CompactParams {
+  char* k;
+  char* v;
+  const int32_t* pos;
+  int32_t* pos_out;
+  int32_t* n_valid;
+  const int32_t* keep;
+  int32_t* dev_status;
+  int64_t slice_bytes;  // bytes between slices
+  int32_t n_cap;
+  int32_t budget;
+  int32_t row_bytes;
+};
+
+struct CalibParams {
+  const void* q;
+  float* ws;
+  float* center;
+  float* mean_norm;
+  float* mrl;
+  int32_t n_q_heads, group, n_split;
+  int32_t kv_heads;
+  int64_t n_tok;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_score(const ScoreParams& p, tri_dtype dt, int head_dim, tri_rope_style style,
+                         bool explicit_pos, int n_slices, cudaStream_t st);
+int score_keys_per_warp_step(tri_dtype dt, int head_dim);
+cudaError_t launch_select(const SelectParams& p, bool random, int n_slices, cudaStream_t st);
+cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st);
+cudaError_t launch_calibrate(const CalibParams& p, tri_dtype dt, int head_dim,
+                             tri_rope_style style, int lh_count, cudaStream_t st);
+int calibrate_split_count(int lh_count, int64_t samples_per_lh);
+
+}  // namespace tri

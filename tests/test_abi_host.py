@@ -1,0 +1,150 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function include/tri.h declares, and rejects bad arguments on the host (these
+calls return before anything touches CUDA, so no GPU is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kv_cache_compression_tri_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    import kv_cache_compression_tri_gb300 as tri
+    return tri.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        txt = open(os.path.join(ROOT, "include", h)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        txt = re.sub(r"//[^\n]*", "", txt)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", txt, flags=re.M):
+            if m.group(1) not in ("if", "while", "for", "return", "sizeof"):
+                names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("tri_calibrate_centers", "tri_score", "tri_select_topk", "tri_compact_kv",
+              "rand_evict", "tri_status_string", "tri_launch_count"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = os.popen(f"nm -D --defined-only {_build.LIB}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in _declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in _declared_functions():
+        getattr(lib, n)
+
+
+def test_status_strings_and_version(lib):
+    for code in range(5):
+        assert lib.tri_status_string(code)
+    assert lib.tri_status_string(99) == b"unknown status"
+    assert lib.tri_abi_version() == 1
+    assert lib.tri_launch_count() >= 0
+
+
+def _kv(**over):
+    import kv_cache_compression_tri_gb300 as tri
+    f = dict(k=0x10000, v=0x20000, pos=None, pos_out=0x30000, n_valid=0x40000, slice_stride=128 * 64,
+             n_seq=1, n_layers=1, n_kv_heads=2, n_cap=128, head_dim=64, dtype=1, dev_status=None)
+    f.update(over)
+    return tri._TriKV(f["k"], f["v"], f["pos"], f["pos_out"], f["n_valid"], f["slice_stride"],
+                      f["n_seq"], f["n_layers"], f["n_kv_heads"], f["n_cap"], f["head_dim"], f["dtype"],
+                      f["dev_status"])
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(head_dim=96), UNSUPPORTED),
+    (dict(dtype=7), UNSUPPORTED),
+    (dict(k=None), INVALID),
+    (dict(k=0x10008), INVALID),  # not 16-byte aligned
+    (dict(n_valid=None), INVALID),
+    (dict(slice_stride=100), INVALID),  # < n_cap * head_dim
+    (dict(slice_stride=128 * 64 + 4), INVALID),  # rows not 16-byte aligned
+    (dict(n_cap=0), INVALID),
+    (dict(n_seq=0), INVALID),
+    (dict(pos_out=None), INVALID),  # compaction needs a position target
+])
+def test_compact_rejects_bad_cache(lib, over, code):
+    kv = _kv(**over)
+    assert lib.tri_compact_kv(ctypes.byref(kv), 0x50000, 64, None) == code
+
+
+def test_select_rejects_bad_budget(lib):
+    kv = _kv()
+    assert lib.tri_select_topk(0x60000, ctypes.byref(kv), 40, 40, 64, 0x50000, None) == INVALID
+    assert lib.tri_select_topk(0x60000, ctypes.byref(kv), -1, 0, 64, 0x50000, None) == INVALID
+    assert lib.tri_select_topk(0x60000, ctypes.byref(kv), 0, 0, 0, 0x50000, None) == INVALID
+    assert lib.tri_select_topk(0x60000, ctypes.byref(kv), 0, 0, 129, 0x50000, None) == INVALID
+    assert lib.tri_select_topk(None, ctypes.byref(kv), 0, 0, 64, 0x50000, None) == INVALID
+    assert lib.tri_select_topk(0x60000, None, 0, 0, 64, 0x50000, None) == INVALID
+    assert lib.rand_evict(ctypes.byref(kv), 0, 0, 40, 40, 64, 0x50000, None) == INVALID
+    assert lib.rand_evict(ctypes.byref(_kv(n_layers=70000)), 0, 0, 0, 0, 64, 0x50000, None) == INVALID
+
+
+def test_score_rejects_bad_args(lib):
+    import kv_cache_compression_tri_gb300 as tri
+    kv = _kv()
+    c = tri._TriCenters(0x70000, 0x80000, 0x90000)
+    offs = (ctypes.c_int32 * 3)(1, 2, 4)
+    op = ctypes.cast(offs, ctypes.c_void_p)
+    call = lambda **o: lib.tri_score(ctypes.byref(o.get("kv", kv)), ctypes.byref(o.get("c", c)),
+                                     o.get("theta", 1e4), o.get("style", 0), o.get("norm", 0),
+                                     o.get("offs", op), o.get("n_off", 3), o.get("p_cur", 0xA0000),
+                                     0, 0, o.get("scores", 0xB0000), None)
+    assert call(theta=0.5) == INVALID
+    assert call(theta=float("nan")) == INVALID
+    assert call(n_off=0) == INVALID
+    assert call(n_off=65) == INVALID
+    assert call(offs=None) == INVALID
+    assert call(style=5) == INVALID
+    assert call(norm=3) == INVALID
+    assert call(p_cur=None) == INVALID
+    assert call(scores=None) == INVALID
+    assert call(kv=_kv(head_dim=256)) == UNSUPPORTED
+    assert call(c=tri._TriCenters(None, 0x80000, 0x90000)) == INVALID
+
+
+def test_calibrate_rejects_bad_args(lib):
+    import kv_cache_compression_tri_gb300 as tri
+    c = tri._TriCenters(0x70000, 0x80000, 0x90000)
+    ws = lib.tri_calibrate_workspace_bytes(2, 8, 4, 128, 4096)
+    assert ws > 0
+    assert lib.tri_calibrate_workspace_bytes(2, 8, 3, 128, 4096) == 0  # 8 % 3 != 0
+    f = lib.tri_calibrate_centers
+    assert f(0x10000, 1, 2, 8, 3, 128, 4096, 0, c, 0xC0000, ws, None) == INVALID
+    assert f(0x10000, 1, 2, 8, 4, 96, 4096, 0, c, 0xC0000, ws, None) == UNSUPPORTED
+    assert f(0x10000, 1, 2, 8, 4, 128, 4096, 0, c, 0xC0000, ws - 1, None) == INVALID
+    assert f(0x10000, 1, 2, 8, 4, 128, 4096, 0, c, None, ws, None) == INVALID
+    assert f(0x10004, 1, 2, 8, 4, 128, 4096, 0, c, 0xC0000, ws, None) == INVALID
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import kv_cache_compression_tri_gb300 as tri
+    monkeypatch.setattr(tri, "_lib", None)
+    monkeypatch.setattr(tri, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        tri.load_library()
+
+
+def test_kv_cache_bytes_worked_example(golden):
+    from kv_cache_compression_tri_gb300.synth import kv_cache_bytes
+    for c in golden("kv_bytes.json")["cases"]:
+        assert kv_cache_bytes(c["layers"], c["d_model"], c["tokens"], c["elem_bytes"], c["batch"]) == c["bytes"]
