@@ -88,8 +88,8 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
-        self.gpu = gpu_index
+    def __init__(self, gpu_id: str, period_ms: int = 100):
+        self.gpu = gpu_id
         self.period = period_ms
         self.proc = None
         self.lines = []
@@ -147,6 +147,30 @@ class ClockSampler:
         med = sm[len(sm) // 2] if sm else None
         return {"sm_mhz": med, "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def nvsmi_gpu_id(torch_index: int) -> str:
+    """nvidia-smi id of a torch device: its UUID (indices may be remapped)."""
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(torch_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        return ids[torch_index] if torch_index < len(ids) else str(torch_index)
+
+
+def host_mem_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 32 << 30
 
 
 def measured_peak_gbs():
@@ -343,7 +367,7 @@ def run_gpu(args, w):
     moved = int((keep_h != np.arange(B)[None, :]).sum())
     restore()
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(nvsmi_gpu_id(local))
     clocks.start()
     time.sleep(0.3)
     recs = [[ev() for _ in range(4)] for _ in range(args.steps)]
@@ -418,15 +442,27 @@ def run_gpu(args, w):
     return 0
 
 
+KERNEL_SOURCES = {"score_kernel": "score.cu", "select_kernel": "select.cu", "compact_kernel": "compact.cu",
+                  "fused_kernel": "fused.cu"}
+
+
 def known_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it covers the
-    current kernel (profiles/traffic.json), else None."""
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    (profiles/traffic.json), or None when there is none or the kernel's
+    source has changed since the counters were taken."""
+    import hashlib
+
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            t = json.load(f)
-        return t.get(workload, {}).get(kernel)
-    except (OSError, ValueError):
+            rec = json.load(f).get(workload, {}).get(kernel)
+        src = os.path.join(ROOT, "kv_cache_compression_tri_gb300", "csrc", KERNEL_SOURCES[kernel])
+        with open(src, "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+    except (OSError, ValueError, KeyError):
         return None
+    if not rec or not sha.startswith(rec.get("source_sha1_prefix", "-")):
+        return None
+    return rec["bytes"]
 
 
 def run_e2e(args, w, tri, synth, inp, centers, dev, stream):
@@ -437,11 +473,7 @@ def run_e2e(args, w, tri, synth, inp, centers, dev, stream):
 
     S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget
     per_seq = 2 * w.n_layers * w.n_kv_heads * w.n_cap * w.head_dim * w.elem_bytes
-    try:
-        import psutil
-        avail = psutil.virtual_memory().available
-    except Exception:
-        avail = 64 << 30
+    avail = host_mem_available()
     n_seq = max(1, min(w.n_seq, int(0.3 * avail) // per_seq, args.e2e_max_seqs))
     Se = n_seq * w.n_layers * w.n_kv_heads
     hk = torch.empty(n_seq, w.n_layers, w.n_kv_heads, w.n_cap, w.head_dim, dtype=w.dtype, pin_memory=True)

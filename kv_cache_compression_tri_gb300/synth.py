@@ -107,6 +107,13 @@ def scaled(w: Workload, **over) -> Workload:
     return Workload(**d)
 
 
+# Profiling case: the stack with one sequence (288 slices, 2.4 GB of K).
+WORKLOADS["qwen3_8b_stack_1seq"] = scaled(WORKLOADS["qwen3_8b_stack"], name="qwen3_8b_stack_1seq", n_seq=1,
+                                          description="one sequence of the Qwen3-8B-shaped stack")
+WORKLOADS["periodic_1seq"] = scaled(WORKLOADS["periodic_large_batch"], name="periodic_1seq", n_seq=1,
+                                    description="one sequence of the large-batch periodic workload")
+
+
 def _unit_rows(g: torch.Generator, shape, norm: float, device) -> torch.Tensor:
     x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
     return x * (norm / x.norm(dim=-1, keepdim=True))
