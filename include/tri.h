@@ -134,6 +134,33 @@ tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layer
                                  void* ws, size_t ws_bytes, tri_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tri_calibrate_centers_noalloc -- tri_calibrate_centers without scratch.
+ * (The pages have no counterpart: this is a convenience of this library.)
+ * For callers that cannot allocate device memory: a plugin inside an engine
+ * that owns all device memory through its own pool and forbids direct driver
+ * allocations, or latency-critical code that must not call cudaMalloc /
+ * cudaFree because those can synchronise the device and stall other streams.
+ * Same arguments, result and arithmetic as tri_calibrate_centers, minus the
+ * scratch: the partial sums go to a fixed array of
+ * TRI_CALIBRATE_NOALLOC_MAX_SCRATCH_BYTES bytes inside the library, which
+ * every GPU that loads the library holds until the process exits. This call
+ * allocates nothing.
+ *   - Shapes whose scratch (tri_calibrate_workspace_bytes) exceeds the array
+ *     return TRI_ERR_INVALID_ARG before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture begins.
+ *   - All calls share the one array, and each call fully rewrites the part it
+ *     reads, so nothing carries over between calls; but calls whose kernels
+ *     overlap on the GPU (e.g. on two streams without ordering) race on it.
+ * ------------------------------------------------------------------------ */
+#define TRI_CALIBRATE_NOALLOC_MAX_SCRATCH_BYTES (4u * 1024u * 1024u)
+tri_status tri_calibrate_centers_noalloc(const void* q, tri_dtype dtype, int32_t n_layers,
+                                         int32_t n_q_heads, int32_t group, int32_t head_dim,
+                                         int64_t n_tok, tri_rope_style style, tri_centers out,
+                                         tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * tri_score -- offset-averaged TriAttention score of cached keys.
  * For every row i of slice s with n_prompt <= i < n_valid[s] - n_recent
  * (protected rows are not scored and their score entries are left as they
