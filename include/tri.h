@@ -61,6 +61,7 @@ typedef enum {
 #define TRI_DEV_NVALID_OVER_CAP 1 /* n_valid[s] > n_cap: slice skipped            */
 #define TRI_DEV_NAN_SCORE 2       /* a candidate score was NaN (ranked lowest)    */
 #define TRI_DEV_BAD_KEEP 3        /* keep list not ascending / out of range       */
+#define TRI_DEV_TIMEOUT 4         /* a bounded in-kernel wait gave up (~2 s)      */
 
 typedef enum { TRI_F32 = 0, TRI_BF16 = 1 } tri_dtype;
 

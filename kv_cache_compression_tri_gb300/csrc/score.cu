@@ -10,19 +10,24 @@
 // (1/|D|) sum_delta [S_trig(k, age + delta) + S_norm(k)] exactly.
 //
 // Design (HBM-bound streaming):
-//   * each warp streams a contiguous run of rows; a key row is split across
-//     TPK lanes, each lane owning BPT consecutive bands and loading them with
-//     one 16-byte (or two 8-byte) streaming load -- fully coalesced;
-//   * per-lane band constants (W_f, n_f and the rotation state) live in
-//     registers; for implicit positions the rotation e^{i w_f (p_cur - p)} is
-//     advanced by one complex multiply per key (anchored once per warp run
-//     from an exact fixed-point phase); for explicit positions it is
-//     evaluated per key from a 64-bit fixed-point phase;
-//   * U = 8 keys are loaded before any is consumed (memory-level
-//     parallelism), then the U partial sums are reduced across the TPK lanes
-//     with a transposed butterfly (reduce-scatter), which costs U - 1 + ...
-//     shuffles instead of U * log2(TPK), and lands U consecutive scores in
-//     consecutive lanes for one coalesced store.
+//   * one CTA streams a contiguous run of a slice's rows through a 4-stage
+//     ring of 16 KB shared-memory tiles, each filled by one bulk async copy
+//     (TMA, non-tensor) that completes on an mbarrier; thread 0 refills a
+//     stage as soon as the CTA has consumed it, so 64 KB per CTA (192 KB per
+//     SM) are always in flight;
+//   * a key row is split across TPK lanes, each lane owning BPT consecutive
+//     bands (one 16-byte shared load per key); band constants live in
+//     registers as fp32 pairs so that two bands share one paired
+//     (f32x2) multiply-add;
+//   * for implicit positions the rotation e^{i w_f (p_cur - p)} is advanced
+//     by one complex multiply per key (anchored once per CTA from an exact
+//     64-bit fixed-point phase); with explicit positions it is evaluated per
+//     key from the fixed-point phase;
+//   * each warp handles RPW rows of a tile as STEPS keys per lane; the STEPS
+//     partial sums are reduced across the TPK lanes with a transposed
+//     butterfly that leaves consecutive scores in consecutive lanes.
+// Every wait on a tile is bounded in wall-clock time; a timeout records
+// TRI_DEV_TIMEOUT, drains the copies in flight and leaves the tile unscored.
 #include <cuda_runtime.h>
 
 #include "tri_internal.cuh"
@@ -32,28 +37,34 @@ namespace {
 
 constexpr int SCORE_THREADS = 256;
 constexpr int SCORE_WARPS = SCORE_THREADS / 32;
-constexpr int U = 8;  // keys in flight per lane per batch
+constexpr int STAGES = 4;
+constexpr int TILE_BYTES = 16384;
+constexpr size_t SCORE_SMEM = STAGES * TILE_BYTES + STAGES * sizeof(uint64_t) + 16;
 
 template <typename T, int D>
-struct Layout {
+struct Geo {
   static constexpr int F = D / 2;
   static constexpr int BPT = (sizeof(T) == 2) ? 4 : 2;  // bands per lane (16 bytes)
   static constexpr int TPK = F / BPT;                   // lanes per key
   static constexpr int KPW = 32 / TPK;                  // keys per warp step
-  static_assert(TPK >= U && TPK <= 32, "layout");
+  static constexpr int ROW_BYTES = D * static_cast<int>(sizeof(T));
+  static constexpr int TILE_ROWS = TILE_BYTES / ROW_BYTES;
+  static constexpr int RPW = TILE_ROWS / SCORE_WARPS;  // rows per warp per tile
+  static constexpr int STEPS = RPW / KPW;              // keys per lane per tile
+  static_assert(STEPS == 4 && TPK >= STEPS && TPK <= 32, "score geometry");
 };
 
-// 16 bytes of one key row for lane group c: interleaved -> one 16-byte load
-// of BPT (re, im) pairs; half-split -> 8 bytes of real parts and 8 bytes of
-// imaginary parts.
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// 16 bytes of one key row for lane group c, from shared memory.
 template <typename T, int D, int STYLE>
-__device__ __forceinline__ uint4 load_chunk(const T* row, int c) {
+__device__ __forceinline__ uint4 lds_chunk(const unsigned char* row, int c) {
   if (STYLE == TRI_ROPE_INTERLEAVED) {
-    return __ldcs(reinterpret_cast<const uint4*>(row) + c);
+    return reinterpret_cast<const uint4*>(row)[c];
   } else {
-    constexpr int F = D / 2;
-    const uint2 a = __ldcs(reinterpret_cast<const uint2*>(row) + c);
-    const uint2 b = __ldcs(reinterpret_cast<const uint2*>(row + F) + c);
+    constexpr int HALF = D * static_cast<int>(sizeof(T)) / 2;
+    const uint2 a = reinterpret_cast<const uint2*>(row)[c];
+    const uint2 b = reinterpret_cast<const uint2*>(row + HALF)[c];
     return make_uint4(a.x, a.y, b.x, b.y);
   }
 }
@@ -81,15 +92,15 @@ __device__ __forceinline__ void decode_chunk(uint4 w, float* re, float* im) {
   }
 }
 
-// Reduce-scatter of a[0..U) over the TPK lanes of one key group. On return,
-// every lane holds the full sum of entry `idx` (lanes that differ only in
-// the bits below TPK/U hold the same entry).
-template <int TPK>
-__device__ __forceinline__ float reduce_scatter(float (&a)[U], int lane, int& idx) {
+// Reduce-scatter of a[0..NU) over the TPK lanes of one key group. On return,
+// every lane holds the full sum of entry `idx` (lanes that differ only in the
+// bits below TPK/NU hold the same entry).
+template <int TPK, int NU>
+__device__ __forceinline__ float reduce_scatter(float (&a)[NU], int lane, int& idx) {
   idx = 0;
   int m = TPK / 2;
 #pragma unroll
-  for (int v = U; v > 1; v >>= 1) {
+  for (int v = NU; v > 1; v >>= 1) {
     const bool upper = (lane & m) != 0;
 #pragma unroll
     for (int j = 0; j < v / 2; ++j) {
@@ -102,126 +113,219 @@ __device__ __forceinline__ float reduce_scatter(float (&a)[U], int lane, int& id
   }
   float r = a[0];
 #pragma unroll
-  for (int mm = TPK / U / 2; mm >= 1; mm >>= 1) r += __shfl_xor_sync(FULL_MASK, r, mm);
+  for (int mm = TPK / NU / 2; mm >= 1; mm >>= 1) r += __shfl_xor_sync(FULL_MASK, r, mm);
   return r;
 }
 
 template <typename T, int D, int STYLE, bool EXPLICIT_POS>
-__global__ void __launch_bounds__(SCORE_THREADS)
+__global__ void __launch_bounds__(SCORE_THREADS, 3)
     score_kernel(const __grid_constant__ ScoreParams p) {
-  using LY = Layout<T, D>;
-  constexpr int F = LY::F, BPT = LY::BPT, TPK = LY::TPK, KPW = LY::KPW;
+  using G = Geo<T, D>;
+  constexpr int F = G::F, BPT = G::BPT, NP = BPT / 2, TPK = G::TPK, KPW = G::KPW;
+  constexpr int ROW_BYTES = G::ROW_BYTES, TILE_ROWS = G::TILE_ROWS, RPW = G::RPW, STEPS = G::STEPS;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
+  volatile int* failed = reinterpret_cast<volatile int*>(full + STAGES);
 
   const int64_t s = blockIdx.x / p.tiles_per_slice;
-  const int tile = blockIdx.x % p.tiles_per_slice;
+  const int ct = blockIdx.x % p.tiles_per_slice;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int n = p.n_valid[s];
+  const int n = p.n_valid[s];
   if (n > p.n_cap || n < 0) {
-    if (threadIdx.x == 0 && tile == 0) set_status(p.dev_status, TRI_DEV_NVALID_OVER_CAP);
+    if (threadIdx.x == 0 && ct == 0) set_status(p.dev_status, TRI_DEV_NVALID_OVER_CAP);
     return;
   }
-  const int lo = p.n_prompt, hi = n - p.n_recent;
-  const int64_t rpc = static_cast<int64_t>(p.rows_per_warp) * SCORE_WARPS;
-  int r0 = static_cast<int>(tile * rpc) + warp * p.rows_per_warp;
-  int r1 = r0 + p.rows_per_warp;
-  r0 = max(r0, lo);
-  r1 = min(r1, hi);
-  if (r0 >= r1) return;  // warp-uniform; no block-level sync below
+  const int c0 = max(ct * p.rows_per_cta, p.n_prompt);
+  const int c1 = min((ct + 1) * p.rows_per_cta, n - p.n_recent);
+  if (c0 >= c1) return;  // uniform over the CTA
+  const int ntiles = (c1 - c0 + TILE_ROWS - 1) / TILE_ROWS;
+  const unsigned char* src =
+      static_cast<const unsigned char*>(p.k) + (s * p.slice_stride + static_cast<int64_t>(c0) * D) * sizeof(T);
 
+  auto issue = [&](int u) {
+    const int rows = min(TILE_ROWS, c1 - c0 - u * TILE_ROWS);
+    const uint32_t bytes = static_cast<uint32_t>(rows * ROW_BYTES);
+    uint64_t* bar = &full[u % STAGES];
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(ring + (u % STAGES) * TILE_BYTES, src + static_cast<int64_t>(u) * TILE_BYTES, bytes, bar);
+  };
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int st = 0; st < STAGES; ++st) mbar_init(&full[st], 1);
+    *failed = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int u = 0; u < min(STAGES, ntiles); ++u) issue(u);
+  }
+
+  // ---- per-lane band constants (bands c*BPT .. c*BPT+BPT-1, as NP pairs) --
   const int c = lane % TPK;   // band group of this lane
   const int kq = lane / TPK;  // key of the warp step this lane works on
   const int lh = static_cast<int>(s % p.lh_count);
   const int64_t seq = s / p.lh_count;
   const int64_t pc = p.p_cur[seq];
-
-  // Per-lane band constants.
-  float2 W[BPT], Dr[BPT], step[BPT];
-  float nw[BPT];
+  float2 WR[NP], WI[NP], DR[NP], DI[NP], SR[NP], SI[NP], NSI[NP], JR[NP], JI[NP], NW[NP];
   uint64_t nu[BPT];
 #pragma unroll
-  for (int b = 0; b < BPT; ++b) {
-    const int f = c * BPT + b;
-    const float2 cf = reinterpret_cast<const float2*>(p.center)[static_cast<int64_t>(lh) * F + f];
-    const float m = p.mean_norm[static_cast<int64_t>(lh) * F + f];
-    const float R = p.mrl[static_cast<int64_t>(lh) * F + f];
-    nw[b] = (p.norm_mode == TRI_NORM_UNWEIGHTED) ? m : (1.0f - R) * m;
-    W[b] = cmul(cf, make_float2(p.g_re[f], p.g_im[f]));
-    nu[b] = p.nu[f];
-    step[b] = make_float2(p.step_re[f], p.step_im[f]);
-    if (!EXPLICIT_POS) Dr[b] = cmul(W[b], turns_rotation_accurate(pc - (r0 + kq), nu[b]));
+  for (int q = 0; q < NP; ++q) {
+    float wr[2], wi[2], nw[2], dr[2], di[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int f = c * BPT + 2 * q + h;
+      const float2 cf = reinterpret_cast<const float2*>(p.center)[static_cast<int64_t>(lh) * F + f];
+      const float m = p.mean_norm[static_cast<int64_t>(lh) * F + f];
+      const float R = p.mrl[static_cast<int64_t>(lh) * F + f];
+      nw[h] = (p.norm_mode == TRI_NORM_UNWEIGHTED) ? m : (1.0f - R) * m;
+      const float2 w = cmul(cf, make_float2(p.g_re[f], p.g_im[f]));
+      wr[h] = w.x;
+      wi[h] = w.y;
+      nu[2 * q + h] = p.nu[f];
+      if (!EXPLICIT_POS) {
+        const float2 d = cmul(w, turns_rotation_accurate(pc - (c0 + warp * RPW + kq), p.nu[f]));
+        dr[h] = d.x;
+        di[h] = d.y;
+      }
+    }
+    WR[q] = f2(wr[0], wr[1]);
+    WI[q] = f2(wi[0], wi[1]);
+    NW[q] = f2(nw[0], nw[1]);
+    const int f0 = c * BPT + 2 * q;
+    SR[q] = f2(p.step_re[f0], p.step_re[f0 + 1]);
+    SI[q] = f2(p.step_im[f0], p.step_im[f0 + 1]);
+    NSI[q] = f2(-p.step_im[f0], -p.step_im[f0 + 1]);
+    JR[q] = f2(p.jump_re[f0], p.jump_re[f0 + 1]);
+    JI[q] = f2(p.jump_im[f0], p.jump_im[f0 + 1]);
+    if (!EXPLICIT_POS) {
+      DR[q] = f2(dr[0], dr[1]);
+      DI[q] = f2(di[0], di[1]);
+    } else {
+      DR[q] = DI[q] = f2(0.f, 0.f);
+    }
   }
 
-  const T* kbase = static_cast<const T*>(p.k) + s * p.slice_stride;
   float* out = p.scores + s * static_cast<int64_t>(p.n_cap);
   const int32_t* pos = EXPLICIT_POS ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
 
-  for (int base = r0; base < r1; base += U * KPW) {
-    uint4 raw[U];
-    int pp[U];
+  int t = 0;
+  for (; t < ntiles; ++t) {
+    const int st = t % STAGES;
+    bool ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((t / STAGES) & 1));
+    ok = __all_sync(FULL_MASK, ok);
+    if (!ok) {
+      if (lane == 0) *failed = 1;
+    } else {
+      const unsigned char* tile = ring + st * TILE_BYTES;
+      const int rbase = warp * RPW + kq;  // row within the tile of this lane's first key
+      int pp[STEPS];
+      if (EXPLICIT_POS) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int row = base + u * KPW + kq;
-      raw[u] = make_uint4(0u, 0u, 0u, 0u);
-      pp[u] = 0;
-      if (row < r1) {
-        raw[u] = load_chunk<T, D, STYLE>(kbase + static_cast<int64_t>(row) * D, c);
-        if (EXPLICIT_POS) pp[u] = __ldg(pos + row);
-      }
-    }
-    float acc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float re[BPT], im[BPT];
-      decode_chunk<T, STYLE>(raw[u], re, im);
-      float a = 0.0f;
-#pragma unroll
-      for (int b = 0; b < BPT; ++b) {
-        float2 d;
-        if (EXPLICIT_POS) {
-          d = cmul(W[b], turns_rotation_fast(pc - pp[u], nu[b]));
-        } else {
-          d = Dr[b];
-          Dr[b] = cmul(Dr[b], step[b]);
+        for (int j = 0; j < STEPS; ++j) {
+          const int r = c0 + t * TILE_ROWS + rbase + j * KPW;
+          pp[j] = (r < c1) ? __ldg(pos + r) : 0;
         }
-        a = fmaf(d.x, re[b], a);
-        a = fmaf(d.y, im[b], a);
-        const float sq = fmaf(im[b], im[b], re[b] * re[b]);
-        a = fmaf(nw[b] * sq, rsqrtf(fmaxf(sq, 1e-30f)), a);  // n_f |k_f|
       }
-      acc[u] = a;
+      float acc[STEPS];
+#pragma unroll
+      for (int j = 0; j < STEPS; ++j) {
+        const int rt = rbase + j * KPW;
+        const bool valid = c0 + t * TILE_ROWS + rt < c1;
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) raw = lds_chunk<T, D, STYLE>(tile + rt * ROW_BYTES, c);
+        float re[BPT], im[BPT];
+        decode_chunk<T, STYLE>(raw, re, im);
+        float2 a2 = f2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+          const float2 RE = f2(re[2 * q], re[2 * q + 1]);
+          const float2 IM = f2(im[2 * q], im[2 * q + 1]);
+          float2 dr, di;
+          if (EXPLICIT_POS) {
+            const float2 r0 = turns_rotation_fast(pc - pp[j], nu[2 * q]);
+            const float2 r1 = turns_rotation_fast(pc - pp[j], nu[2 * q + 1]);
+            const float2 C = f2(r0.x, r1.x), S = f2(r0.y, r1.y);
+            dr = __ffma2_rn(WR[q], C, __fmul2_rn(WI[q], f2(-S.x, -S.y)));
+            di = __ffma2_rn(WR[q], S, __fmul2_rn(WI[q], C));
+          } else {
+            dr = DR[q];
+            di = DI[q];
+            DR[q] = __ffma2_rn(dr, SR[q], __fmul2_rn(di, NSI[q]));
+            DI[q] = __ffma2_rn(dr, SI[q], __fmul2_rn(di, SR[q]));
+          }
+          a2 = __ffma2_rn(dr, RE, a2);
+          a2 = __ffma2_rn(di, IM, a2);
+          const float2 sq = __ffma2_rn(IM, IM, __fmul2_rn(RE, RE));
+          a2 = __ffma2_rn(NW[q], f2(sqrt_approx(sq.x), sqrt_approx(sq.y)), a2);
+        }
+        acc[j] = a2.x + a2.y;
+      }
+      if (!EXPLICIT_POS) {
+        // from this lane's last key of tile t to its first key of tile t + 1
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+          const float2 dr = DR[q], di = DI[q];
+          const float2 nji = f2(-JI[q].x, -JI[q].y);
+          DR[q] = __ffma2_rn(dr, JR[q], __fmul2_rn(di, nji));
+          DI[q] = __ffma2_rn(dr, JI[q], __fmul2_rn(di, JR[q]));
+        }
+      }
+      int idx;
+      const float v = reduce_scatter<TPK, STEPS>(acc, lane, idx);
+      const int r = c0 + t * TILE_ROWS + rbase + idx * KPW;
+      if ((c % (TPK / STEPS)) == 0 && r < c1) __stcs(out + r, v);
     }
-    int idx;
-    const float v = reduce_scatter<TPK>(acc, lane, idx);
-    const int row = base + idx * KPW + kq;
-    if ((c % (TPK / U)) == 0 && row < r1) __stcs(out + row, v);
+    __syncthreads();  // the whole CTA is done with stage st
+    if (*failed) break;
+    if (threadIdx.x == 0 && t + STAGES < ntiles) {
+      fence_proxy_async_smem();
+      issue(t + STAGES);
+    }
+  }
+  if (t < ntiles && threadIdx.x == 0) {
+    // A wait timed out: report it and let the copies already in flight land
+    // before the CTA's shared memory is released.
+    set_status(p.dev_status, TRI_DEV_TIMEOUT);
+    for (int u = t; u < min(ntiles, t + STAGES); ++u)
+      (void)mbar_wait_bounded(&full[u % STAGES], static_cast<uint32_t>((u / STAGES) & 1));
   }
 }
 
-template <typename T, int D, int STYLE>
-cudaError_t launch_typed(const ScoreParams& p, bool explicit_pos, int n_slices, cudaStream_t st) {
+template <typename T, int D, int STYLE, bool EXPLICIT_POS>
+cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
+  auto kern = score_kernel<T, D, STYLE, EXPLICIT_POS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SCORE_SMEM));
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(n_slices) * p.tiles_per_slice));
-  if (explicit_pos)
-    score_kernel<T, D, STYLE, true><<<grid, SCORE_THREADS, 0, st>>>(p);
-  else
-    score_kernel<T, D, STYLE, false><<<grid, SCORE_THREADS, 0, st>>>(p);
+  kern<<<grid, SCORE_THREADS, SCORE_SMEM, st>>>(p);
   note_launch();
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-cudaError_t launch_style(const ScoreParams& p, tri_rope_style style, bool explicit_pos,
-                         int n_slices, cudaStream_t st) {
+cudaError_t launch_style(const ScoreParams& p, tri_rope_style style, bool explicit_pos, int n_slices,
+                         cudaStream_t st) {
   if (style == TRI_ROPE_INTERLEAVED)
-    return launch_typed<T, D, TRI_ROPE_INTERLEAVED>(p, explicit_pos, n_slices, st);
-  return launch_typed<T, D, TRI_ROPE_HALF>(p, explicit_pos, n_slices, st);
+    return explicit_pos ? launch_one<T, D, TRI_ROPE_INTERLEAVED, true>(p, n_slices, st)
+                        : launch_one<T, D, TRI_ROPE_INTERLEAVED, false>(p, n_slices, st);
+  return explicit_pos ? launch_one<T, D, TRI_ROPE_HALF, true>(p, n_slices, st)
+                      : launch_one<T, D, TRI_ROPE_HALF, false>(p, n_slices, st);
+}
+
+template <typename T, int D>
+ScoreGeometry geo() {
+  using G = Geo<T, D>;
+  return ScoreGeometry{G::KPW, G::TILE_ROWS - G::RPW, G::TILE_ROWS};
 }
 
 }  // namespace
 
-int score_keys_per_warp_step(tri_dtype dt, int head_dim) {
-  const int bpt = (dt == TRI_BF16) ? 4 : 2;
-  return 32 / ((head_dim / 2) / bpt);
+ScoreGeometry score_geometry(tri_dtype dt, int head_dim) {
+  if (dt == TRI_BF16) return head_dim == 128 ? geo<uint16_t, 128>() : geo<uint16_t, 64>();
+  return head_dim == 128 ? geo<float, 128>() : geo<float, 64>();
 }
 
 cudaError_t launch_score(const ScoreParams& p, tri_dtype dt, int head_dim, tri_rope_style style,

@@ -139,7 +139,7 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
 
   ScoreParams p{};
   const int D = kv->head_dim, F = D / 2;
-  const int kpw = score_keys_per_warp_step(kv->dtype, D);
+  const ScoreGeometry g = score_geometry(kv->dtype, D);
   for (int f = 0; f < F; ++f) {
     const double omega = std::pow(rope_theta, -2.0 * f / D);
     p.nu[f] = nu_fixed(omega);
@@ -150,8 +150,10 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
     }
     p.g_re[f] = static_cast<float>(gr / n_offsets);
     p.g_im[f] = static_cast<float>(gi / n_offsets);
-    p.step_re[f] = static_cast<float>(std::cos(omega * kpw));
-    p.step_im[f] = static_cast<float>(-std::sin(omega * kpw));
+    p.step_re[f] = static_cast<float>(std::cos(omega * g.step));
+    p.step_im[f] = static_cast<float>(-std::sin(omega * g.step));
+    p.jump_re[f] = static_cast<float>(std::cos(omega * g.jump));
+    p.jump_im[f] = static_cast<float>(-std::sin(omega * g.jump));
   }
   p.k = kv->k;
   p.pos = kv->pos;
@@ -168,16 +170,12 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
   p.n_prompt = n_prompt;
   p.n_recent = n_recent;
   p.norm_mode = norm_mode;
-  // ~512 KB of keys per CTA: 8 warps x rows_per_warp rows (a multiple of the
-  // warp's 8-key batch).
-  const int row_bytes = D * elem_bytes(kv->dtype);
-  int rpw = (512 * 1024 / row_bytes) / 8;
-  const int batch = 8 * kpw;
-  rpw = ((rpw + batch - 1) / batch) * batch;
-  const int cap_rpw = ((kv->n_cap + 7) / 8 + batch - 1) / batch * batch;  // small caches
-  if (cap_rpw < rpw) rpw = cap_rpw;
-  p.rows_per_warp = rpw;
-  p.tiles_per_slice = static_cast<int32_t>((kv->n_cap + 8LL * rpw - 1) / (8LL * rpw));
+  // ~512 KB of keys per CTA (32 tiles), fewer for small caches.
+  int rpc = 32 * g.tile_rows;
+  const int cap_rows = (kv->n_cap + g.tile_rows - 1) / g.tile_rows * g.tile_rows;
+  if (cap_rows < rpc) rpc = cap_rows;
+  p.rows_per_cta = rpc;
+  p.tiles_per_slice = static_cast<int32_t>((kv->n_cap + rpc - 1) / rpc);
   const int64_t grid = slices_of(kv) * p.tiles_per_slice;
   if (grid > 0x7fffffff) return TRI_ERR_INVALID_ARG;
   const cudaError_t e = launch_score(p, kv->dtype, D, style, kv->pos != nullptr,

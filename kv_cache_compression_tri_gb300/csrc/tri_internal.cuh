@@ -69,6 +69,81 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint2 key) {
   return x;
 }
 
+// ---------------------------------------------------------------------------
+// Bulk async copies (TMA, non-tensor) into shared memory with mbarrier
+// completion, and a wall-clock-bounded wait.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Order this thread's earlier shared-memory accesses before later async-proxy
+// writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned); completion is counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  uint64_t gsrc;
+  asm volatile("cvta.to.global.u64 %0, %1;" : "=l"(gsrc) : "l"(src));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of `bar`; gives up after ~2 s of wall clock so a
+// lost completion can never hang the GPU (the caller reports TRI_DEV_TIMEOUT).
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+
+// sqrt of a non-negative fp32 (hardware approximation; exact at 0).
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float r;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Order-preserving map of an fp32 score to u32 (larger score -> larger key).
 // -0 is folded onto +0; NaN maps to 0 (below every number) and is flagged.
 __device__ __forceinline__ uint32_t score_key(float x, bool& nan) {
@@ -99,13 +174,15 @@ struct ScoreParams {
   int32_t lh_count;  // n_layers * n_kv_heads
   int32_t n_prompt, n_recent;
   int32_t norm_mode;
-  int32_t tiles_per_slice;
-  int32_t rows_per_warp;
+  int32_t tiles_per_slice;  // CTAs per slice
+  int32_t rows_per_cta;
   uint64_t nu[MAX_BANDS];     // omega_f / 2pi as 0.64 fixed point (turns per position)
   float g_re[MAX_BANDS];      // G_f = (1/|D|) sum_delta e^{i omega_f delta}
   float g_im[MAX_BANDS];
-  float step_re[MAX_BANDS];   // e^{-i omega_f * (keys per warp step)}
+  float step_re[MAX_BANDS];   // e^{-i omega_f * (positions between a lane's keys in a tile)}
   float step_im[MAX_BANDS];
+  float jump_re[MAX_BANDS];   // e^{-i omega_f * (positions skipped between tiles)}
+  float jump_im[MAX_BANDS];
 };
 
 struct SelectParams {
@@ -147,7 +224,15 @@ struct CalibParams {
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_score(const ScoreParams& p, tri_dtype dt, int head_dim, tri_rope_style style,
                          bool explicit_pos, int n_slices, cudaStream_t st);
-int score_keys_per_warp_step(tri_dtype dt, int head_dim);
+// Score kernel geometry, shared by the launcher and the host constant table:
+// positions between consecutive keys of one lane inside a tile, and the
+// positions skipped from a lane's last key of a tile to its first of the next.
+struct ScoreGeometry {
+  int step;
+  int jump;
+  int tile_rows;
+};
+ScoreGeometry score_geometry(tri_dtype dt, int head_dim);
 cudaError_t launch_select(const SelectParams& p, bool random, int n_slices, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_calibrate(const CalibParams& p, tri_dtype dt, int head_dim,
