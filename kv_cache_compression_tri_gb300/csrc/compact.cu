@@ -2,19 +2,25 @@
 //
 // Random Attention, Appendix F: keep-sets are sorted chronologically and the
 // KV tensors are compacted with a gather. Semantics: for j = 0, 1, ...,
-// n_keep-1 in order, row j <- row keep[j]. Because keep is ascending with
-// keep[j] >= j, the source of destination j is never a row written by an
-// earlier destination, but it may be a row that a LATER destination
-// overwrites (keep = {1, 2, ...}). One CTA owns one (slice, tensor) and
-// walks destination tiles of TR rows in ascending order:
-//   read(tile t)  ->  barrier  ->  write(tile t)
-// All sources of tile t are read before any row of tile t is written (the
-// barrier), and every row written by tile t (< (t+1) TR) is below every
-// source of later tiles (>= (t+1) TR). So the reads of tile t+1 may be
-// issued before the writes of tile t: they are double-buffered in
-// registers, keeping a tile of loads in flight while the previous tile
-// drains. Identity rows (keep[j] == j, e.g. the protected prompt) are
-// neither read nor written.
+// n_keep-1 in order, row j <- row keep[j]. keep is ascending with
+// keep[j] >= j, so the source of destination j is never a row written by an
+// earlier destination, though it may be a row that a later destination
+// overwrites (keep = {1, 2, ...}).
+//
+// One CTA owns one (slice, tensor). After validating the keep list (and, for
+// the K CTA, moving the positions), one warp moves the rows through a
+// 4-stage ring of 8 KB shared-memory tiles:
+//   * tile u (destination rows [u*TR, (u+1)*TR)) is gathered row by row with
+//     bulk async copies (TMA, non-tensor) completing on the stage's mbarrier;
+//   * once it has landed it is written back with ONE bulk store: past the
+//     identity prefix (keep[j] == j, e.g. the protected prompt, which is
+//     neither read nor written) every destination row moves, so a tile's
+//     destinations are contiguous;
+//   * the store of tile u overlaps the gathers of tiles u+1..u+3. This is
+//     safe: every source of a later tile is >= (u+1)*TR, above every row tile
+//     u writes, and tile u's own sources were read before its store was
+//     issued.
+// Waits on gathers are bounded in wall-clock time (TRI_DEV_TIMEOUT).
 #include <cuda_runtime.h>
 
 #include "tri_internal.cuh"
@@ -22,8 +28,11 @@
 namespace tri {
 namespace {
 
-constexpr int CT = 256;  // threads per CTA
-constexpr int CU = 4;    // 16-byte items per thread per tile
+constexpr int CT = 128;  // threads per CTA (validation, positions); warp 0 moves rows
+constexpr int CSTAGES = 4;
+constexpr int CTILE = 8192;
+constexpr size_t COMPACT_SMEM = CSTAGES * CTILE + CSTAGES * sizeof(uint64_t);
+constexpr int POS_PER_THREAD = 8;
 
 struct CSmem {
   int bad;
@@ -31,11 +40,12 @@ struct CSmem {
   int first_move;
 };
 
-template <int CHUNKS>  // 16-byte chunks per row
 __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ CompactParams p) {
-  constexpr int TR = CT * CU / CHUNKS;  // rows per tile
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + CSTAGES * CTILE);
   __shared__ CSmem sm;
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31;
   const int64_t s = blockIdx.x;
   const bool is_k = (blockIdx.y == 0);
   const int32_t* keep = p.keep + s * static_cast<int64_t>(p.budget);
@@ -48,13 +58,13 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   __syncthreads();
   // Validate the keep list before touching anything: ascending, keep[j] >= j,
   // < n_cap, and -1 only as trailing padding.
+#pragma unroll 4
   for (int j = t; j < p.budget; j += CT) {
-    const int kj = keep[j];
-    const int prev = (j > 0) ? keep[j - 1] : -2;
+    const int kj = __ldg(keep + j);
+    const int prev = (j > 0) ? __ldg(keep + j - 1) : -2;
     if (kj < 0) {
       if (kj != -1) atomicOr(&sm.bad, 1);
-      if (prev >= 0 || j == 0) atomicMin(&sm.n_keep, j);
-      if (j > 0 && prev == -1) { /* padding continues */ }
+      atomicMin(&sm.n_keep, j);
     } else {
       if (kj < j || kj >= p.n_cap || (j > 0 && (prev < 0 || prev >= kj))) atomicOr(&sm.bad, 1);
       if (kj != j) atomicMin(&sm.first_move, j);
@@ -68,90 +78,107 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   const int n_keep = sm.n_keep;
   const int first = min(sm.first_move, n_keep);
 
+  if (is_k) {
+    int32_t* pos_out = p.pos_out + s * static_cast<int64_t>(p.n_cap);
+    const int32_t* pos_in = p.pos ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
+    if (pos_in == nullptr || pos_in != pos_out) {
+      // distinct buffers (or positions implied by the slot): a plain gather
+      for (int j = t; j < n_keep; j += CT) pos_out[j] = pos_in ? __ldg(pos_in + __ldg(keep + j)) : __ldg(keep + j);
+    } else {
+      // in place: read a chunk's sources, barrier, write it; sources of later
+      // chunks lie above every row written so far
+      for (int c0 = first; c0 < n_keep; c0 += CT * POS_PER_THREAD) {
+        int32_t v[POS_PER_THREAD];
+#pragma unroll
+        for (int e = 0; e < POS_PER_THREAD; ++e) {
+          const int j = c0 + e * CT + t;
+          v[e] = (j < n_keep) ? pos_in[__ldg(keep + j)] : 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < POS_PER_THREAD; ++e) {
+          const int j = c0 + e * CT + t;
+          if (j < n_keep) pos_out[j] = v[e];
+        }
+        __syncthreads();
+      }
+    }
+    if (t == 0) p.n_valid[s] = n_keep;
+  }
+  if (t >= 32 || first >= n_keep) return;
+
+  // ---- warp 0: rows [first, n_keep) through the bulk-copy ring ------------
   char* base = (is_k ? p.k : p.v) + s * p.slice_bytes;
-  const int64_t rb = p.row_bytes;
-  int32_t* pos_out = p.pos_out + s * static_cast<int64_t>(p.n_cap);
-  const int32_t* pos_in = p.pos ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
-  const bool pos_in_place = (pos_in != nullptr) && (pos_in == pos_out);
-
-  // Positions that are not moved in place: a plain gather (or the slot index).
-  if (is_k && !pos_in_place) {
-    for (int j = t; j < n_keep; j += CT) pos_out[j] = pos_in ? pos_in[keep[j]] : keep[j];
+  const int rb = p.row_bytes;
+  const int TR = CTILE / rb;  // rows per tile
+  const int u_first = first / TR;
+  const int ntiles = (n_keep - 1) / TR - u_first + 1;
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < CSTAGES; ++st) mbar_init(&full[st], 1);
+    mbar_init_fence();
   }
+  __syncwarp();
 
-  uint4 A[CU], Bv[CU];
-  int32_t pa = 0, pb = 0;
-  auto read_tile = [&](int t0, uint4 (&buf)[CU], int32_t& pbuf) {
-#pragma unroll
-    for (int u = 0; u < CU; ++u) {
-      const int item = t + u * CT;
-      const int j = t0 + item / CHUNKS;
-      const int ch = item % CHUNKS;
-      if (j < n_keep) {
-        const int kj = keep[j];
-        if (kj != j)
-          buf[u] = __ldcs(reinterpret_cast<const uint4*>(base + kj * rb) + ch);
-      }
-    }
-    if (is_k && pos_in_place && t < TR) {
-      const int j = t0 + t;
-      if (j < n_keep) {
-        const int kj = keep[j];
-        if (kj != j) pbuf = pos_in[kj];
-      }
-    }
+  auto rows_of = [&](int k, int& lo_j, int& hi_j, int& t0) {
+    t0 = (u_first + k) * TR;
+    lo_j = max(t0, first);
+    hi_j = min(t0 + TR, n_keep);
   };
-  auto write_tile = [&](int t0, const uint4 (&buf)[CU], int32_t pbuf) {
-#pragma unroll
-    for (int u = 0; u < CU; ++u) {
-      const int item = t + u * CT;
-      const int j = t0 + item / CHUNKS;
-      const int ch = item % CHUNKS;
-      if (j < n_keep && keep[j] != j)
-        __stcs(reinterpret_cast<uint4*>(base + j * rb) + ch, buf[u]);
-    }
-    if (is_k && pos_in_place && t < TR) {
-      const int j = t0 + t;
-      if (j < n_keep && keep[j] != j) pos_out[j] = pbuf;
+  auto gather = [&](int k) {
+    int lo_j, hi_j, t0;
+    rows_of(k, lo_j, hi_j, t0);
+    const int st = k % CSTAGES;
+    if (lane == 0) mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((hi_j - lo_j) * rb));
+    __syncwarp();
+    for (int j = lo_j + lane; j < hi_j; j += 32) {
+      const int kj = __ldg(keep + j);
+      bulk_g2s(ring + st * CTILE + (j - t0) * rb, base + static_cast<int64_t>(kj) * rb,
+               static_cast<uint32_t>(rb), &full[st]);
     }
   };
 
-  int t0 = (first / TR) * TR;
-  if (t0 < n_keep) {
-    read_tile(t0, A, pa);
-    for (;;) {
-      __syncthreads();  // all reads of tile t0 are performed before its writes
-      if (t0 + TR < n_keep) read_tile(t0 + TR, Bv, pb);
-      write_tile(t0, A, pa);
-      t0 += TR;
-      if (t0 >= n_keep) break;
-      __syncthreads();
-      if (t0 + TR < n_keep) read_tile(t0 + TR, A, pa);
-      write_tile(t0, Bv, pb);
-      t0 += TR;
-      if (t0 >= n_keep) break;
+  for (int k = 0; k < min(CSTAGES - 1, ntiles); ++k) gather(k);
+  int k = 0;
+  bool ok = true;
+  for (; k < ntiles; ++k) {
+    const int st = k % CSTAGES;
+    ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / CSTAGES) & 1));
+    ok = __all_sync(FULL_MASK, ok);
+    if (!ok) break;
+    if (lane == 0) {
+      int lo_j, hi_j, t0;
+      rows_of(k, lo_j, hi_j, t0);
+      bulk_s2g(base + static_cast<int64_t>(lo_j) * rb, ring + st * CTILE + (lo_j - t0) * rb,
+               static_cast<uint32_t>((hi_j - lo_j) * rb));
+      bulk_commit();
+    }
+    const int kn = k + CSTAGES - 1;  // refills the stage of tile k - 1
+    if (kn < ntiles) {
+      if (lane == 0) bulk_wait_read<1>();  // tile k-1's store has read its stage
+      __syncwarp();
+      gather(kn);
     }
   }
-  if (is_k && t == 0) p.n_valid[s] = n_keep;
+  if (!ok && lane == 0) {
+    // A gather never landed: report it and let the copies in flight finish
+    // before the CTA's shared memory is released.
+    set_status(p.dev_status, TRI_DEV_TIMEOUT);
+    for (int u = k; u < min(ntiles, k + CSTAGES - 1); ++u)
+      (void)mbar_wait_bounded(&full[u % CSTAGES], static_cast<uint32_t>((u / CSTAGES) & 1));
+  }
+  if (lane == 0) bulk_wait_all();
 }
 
 }  // namespace
 
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st) {
+  if (p.row_bytes % 16 != 0 || p.row_bytes > CTILE) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(COMPACT_SMEM));
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(n_slices), 2);
-  switch (p.row_bytes / 16) {
-    case 8:
-      compact_kernel<8><<<grid, CT, 0, st>>>(p);
-      break;
-    case 16:
-      compact_kernel<16><<<grid, CT, 0, st>>>(p);
-      break;
-    case 32:
-      compact_kernel<32><<<grid, CT, 0, st>>>(p);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
+  compact_kernel<<<grid, CT, COMPACT_SMEM, st>>>(p);
   note_launch();
   return cudaGetLastError();
 }

@@ -5,19 +5,23 @@
 // draws, prompt forced in): keep [0, P) U top-(B-P-W) candidates U
 // [n-W, n), ascending. One CTA of 1024 threads owns one slice:
 //   1. candidate keys -- the order-preserving u32 of the fp32 score, or the
-//      Philox-4x32-10 draw -- are staged in shared memory (up to 32768 per
-//      pass, 128 KB), slot-ordered;
-//   2. a 4-pass MSD radix select (8-bit digits) finds the exact threshold
-//      key T and how many keys equal to T are still needed; the histogram
-//      lives in shared memory and same-digit lanes are merged with
-//      match.any so a warp issues one shared atomic per distinct digit; the
-//      select stops early when a digit bin is taken whole;
-//   3. one block-wide scan in slot order ranks the kept keys (warp ballots
-//      plus one scan over (chunk, warp) counts), so the keep list comes out
-//      ascending without sorting; among keys equal to T the lower slots win
-//      (a second scan ranks them only when needed).
-// Slices with more than 32768 candidates are processed in 32768-key
-// super-chunks re-staged for every pass (scores re-read, draws recomputed).
+//      Philox-4x32-10 draw -- are staged in shared memory (up to 32768,
+//      128 KB), slot-ordered, while the block finds their min and max;
+//   2. the bits above the highest bit where min and max differ are common to
+//      every key, so the first 8-bit radix digit starts just below them and
+//      spans the keys' real range; one histogram pass over all keys (shared
+//      atomics merged per digit with match.any) finds the digit bin that
+//      holds the k-th largest key;
+//   3. the keys of that bin (a few hundred typically) are collected into a
+//      short list and the remaining digits are resolved on the list only;
+//      the select stops as soon as a bin is taken whole;
+//   4. one block-wide scan in slot order (warp ballots plus one scan over
+//      (chunk, warp) counts) emits the keep list ascending without sorting;
+//      among keys equal to the threshold the lower slots win (ranked by a
+//      second scan only when needed).
+// Slices with more than 32768 candidates, or whose threshold bin does not
+// fit the list, fall back to full-array radix passes (re-staging the keys
+// for every pass when they do not fit shared memory).
 #include <cuda_runtime.h>
 
 #include "tri_internal.cuh"
@@ -29,7 +33,8 @@ constexpr int NT = 1024;
 constexpr int NW = NT / 32;
 constexpr int KCAP = 32768;     // keys staged per super-chunk
 constexpr int NCH = KCAP / NT;  // chunks of NT slots per super-chunk
-constexpr size_t KEY_SMEM = KCAP * sizeof(uint32_t);
+constexpr int LCAP = 4096;      // short-list capacity
+constexpr size_t SEL_SMEM = KCAP * sizeof(uint32_t) + LCAP * (sizeof(uint32_t) + sizeof(int32_t));
 
 struct SliceCtx {
   int64_t s;
@@ -43,36 +48,87 @@ struct Smem {
   unsigned hist[256];
   unsigned tot[NCH * NW];  // per (chunk, warp) counts, then exclusive offsets
   unsigned wsum[NW];
+  unsigned wmin[NW], wmax[NW];
   unsigned total;
   int pick_digit;
   unsigned pick_above, pick_count;
+  unsigned nlist;
   int nan_seen;
 };
 
 // Stage the keys of slots [base, base + KCAP) into skey (slot-ordered).
 // Slots outside [P, end) get key 0 and are masked out by their index later.
+// Returns this thread's min / max over the valid keys it staged.
 template <bool RANDOM>
 __device__ __forceinline__ void stage_keys(const SelectParams& p, const SliceCtx& c, int base,
-                                           uint32_t* skey, bool& nan) {
+                                           uint32_t* skey, bool& nan, uint32_t& kmin, uint32_t& kmax) {
   if (RANDOM) {
     // one Philox call yields the draws of 4 consecutive slots (base % 4 == 0)
     const uint2 key = make_uint2(static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
     const uint32_t lay = static_cast<uint32_t>(c.head + 65536 * c.layer);
+#pragma unroll 2
     for (int g = threadIdx.x; g < KCAP / 4; g += NT) {
       const int i0 = base + 4 * g;
       uint4 r = make_uint4(0u, 0u, 0u, 0u);
       if (i0 < c.end)
         r = philox4x32_10(
             make_uint4(static_cast<uint32_t>(i0) >> 2, lay, static_cast<uint32_t>(c.seq), p.round), key);
+      const uint32_t v[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool valid = (i0 + e >= c.P) && (i0 + e < c.end);
+        if (valid) {
+          kmin = min(kmin, v[e]);
+          kmax = max(kmax, v[e]);
+        }
+      }
       reinterpret_cast<uint4*>(skey)[g] = r;
     }
   } else {
     const float* row = p.scores + c.s * static_cast<int64_t>(p.n_cap);
-    for (int j = threadIdx.x; j < KCAP; j += NT) {
-      const int i = base + j;
-      uint32_t k = 0u;
-      if (i >= c.P && i < c.end) k = score_key(__ldcg(row + i), nan);
-      skey[j] = k;
+    if (((c.s * static_cast<int64_t>(p.n_cap) + base) & 3) == 0) {
+      // 16-byte loads, all issued before any is used
+      constexpr int PER = KCAP / 4 / NT;
+      float4 v[PER];
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int i0 = base + 4 * (q * NT + threadIdx.x);
+        if (i0 + 3 < c.end) {
+          v[q] = __ldcg(reinterpret_cast<const float4*>(row + i0));
+        } else {
+          v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (i0 < c.end) v[q].x = __ldcg(row + i0);
+          if (i0 + 1 < c.end) v[q].y = __ldcg(row + i0 + 1);
+          if (i0 + 2 < c.end) v[q].z = __ldcg(row + i0 + 2);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int i0 = base + 4 * (q * NT + threadIdx.x);
+        const float f[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+        uint32_t k[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool valid = (i0 + e >= c.P) && (i0 + e < c.end);
+          k[e] = valid ? score_key(f[e], nan) : 0u;
+          if (valid) {
+            kmin = min(kmin, k[e]);
+            kmax = max(kmax, k[e]);
+          }
+        }
+        reinterpret_cast<uint4*>(skey)[q * NT + threadIdx.x] = make_uint4(k[0], k[1], k[2], k[3]);
+      }
+    } else {
+      for (int j = threadIdx.x; j < KCAP; j += NT) {
+        const int i = base + j;
+        uint32_t k = 0u;
+        if (i >= c.P && i < c.end) {
+          k = score_key(__ldcg(row + i), nan);
+          kmin = min(kmin, k);
+          kmax = max(kmax, k);
+        }
+        skey[j] = k;
+      }
     }
   }
 }
@@ -122,9 +178,50 @@ __device__ __forceinline__ unsigned chunk_offsets(Smem& sm, uint32_t bits, int l
   return block_exclusive_scan(sm, NCH * NW);
 }
 
+// Add one key to the digit histogram; lanes with the same digit are merged
+// so each distinct digit costs one shared atomic per warp.
+__device__ __forceinline__ void hist_add(Smem& sm, bool act, unsigned digit, int lane) {
+  const unsigned d = act ? digit : 256u;
+  const unsigned peers = __match_any_sync(FULL_MASK, d);
+  if (act && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], __popc(peers));
+}
+
+// Warp 0 finds digit b with count(digits > b) < need <= count(digits >= b)
+// and publishes (b, count above b, count of b). Caller syncs around it.
+__device__ __forceinline__ void pick_bin(Smem& sm, unsigned need, int lane) {
+  unsigned h[8], ls = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    h[j] = sm.hist[lane * 8 + j];
+    ls += h[j];
+  }
+  unsigned suf = ls;  // inclusive suffix sum over lanes >= this lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_down_sync(FULL_MASK, suf, o);
+    if (lane + o < 32) suf += y;
+  }
+  const unsigned above_lane = suf - ls;
+  if (above_lane < need && need <= suf) {
+    unsigned cum = above_lane;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      if (cum + h[j] >= need) {
+        sm.pick_digit = lane * 8 + j;
+        sm.pick_above = cum;
+        sm.pick_count = h[j];
+        break;
+      }
+      cum += h[j];
+    }
+  }
+}
+
 template <bool RANDOM>
 __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(16) uint32_t skey[];
+  uint32_t* lkey = skey + KCAP;
+  int32_t* lslot = reinterpret_cast<int32_t*>(lkey + LCAP);
   __shared__ Smem sm;
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -157,24 +254,63 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
 
   const int n_super = (c.end - c.lo + KCAP - 1) / KCAP;
   const bool staged_once = (n_super == 1);
-  if (t == 0) sm.nan_seen = 0;
+  if (t == 0) {
+    sm.nan_seen = 0;
+    sm.nlist = 0u;
+  }
   bool nan = false;
+  uint32_t prefix = 0u, mask = 0u;
+  int shift = 24;  // lowest bit of the next digit
+  int width = 8;   // bits of the next digit
+  unsigned need = static_cast<unsigned>(need_total);
+  bool exact = false, resolved = false;
+
   if (staged_once) {
-    stage_keys<RANDOM>(p, c, c.lo, skey, nan);
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    stage_keys<RANDOM>(p, c, c.lo, skey, nan, kmin, kmax);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(FULL_MASK, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(FULL_MASK, kmax, o));
+    }
+    if (lane == 0) {
+      sm.wmin[w] = kmin;
+      sm.wmax[w] = kmax;
+    }
     __syncthreads();
+    kmin = sm.wmin[lane];
+    kmax = sm.wmax[lane];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(FULL_MASK, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(FULL_MASK, kmax, o));
+    }
+    // every thread now holds the block min and max
+    const uint32_t diff = kmin ^ kmax;
+    if (diff == 0u) {
+      prefix = kmin;  // all candidates equal: lowest slots win
+      mask = 0xffffffffu;
+      resolved = true;
+    } else {
+      const int hb = 31 - __clz(diff);
+      shift = max(hb - 7, 0);
+      width = hb - shift + 1;
+      mask = (hb == 31) ? 0u : ~((2u << hb) - 1u);  // bits above hb: common to all keys
+      prefix = kmin & mask;
+    }
   }
 
-  // ---- radix select: 4 passes of 8 bits, most significant first ----------
-  uint32_t prefix = 0u, mask = 0u;
-  unsigned need = static_cast<unsigned>(need_total);
-  bool exact = false;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  // ---- radix passes over the full key array -------------------------------
+  // (once when staged in shared memory; until resolved when streaming)
+  while (!resolved) {
     if (t < 256) sm.hist[t] = 0u;
     __syncthreads();
+    const uint32_t dmask = (1u << width) - 1u;
     for (int sc = 0; sc < n_super; ++sc) {
       const int base = c.lo + sc * KCAP;
       if (!staged_once) {
-        stage_keys<RANDOM>(p, c, base, skey, nan);
+        uint32_t a = 0xffffffffu, b = 0u;
+        stage_keys<RANDOM>(p, c, base, skey, nan, a, b);
         __syncthreads();
       }
       for (int q = 0; q < NCH; ++q) {
@@ -182,52 +318,78 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
         const int i = base + j;
         const uint32_t k = skey[j];
         const bool act = (i >= c.P) && (i < c.end) && ((k & mask) == prefix);
-        const unsigned digit = act ? ((k >> shift) & 0xffu) : 256u;
-        const unsigned peers = __match_any_sync(FULL_MASK, digit);
-        if (act && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], __popc(peers));
+        hist_add(sm, act, (k >> shift) & dmask, lane);
       }
       if (!staged_once) __syncthreads();  // skey is re-staged next
     }
     __syncthreads();
-    if (w == 0) {
-      // digit b with count(digits > b) < need <= count(digits >= b)
-      unsigned h[8], ls = 0u;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        h[j] = sm.hist[lane * 8 + j];
-        ls += h[j];
-      }
-      unsigned suf = ls;  // inclusive suffix sum over lanes >= this lane
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_down_sync(FULL_MASK, suf, o);
-        if (lane + o < 32) suf += y;
-      }
-      const unsigned above_lane = suf - ls;
-      if (above_lane < need && need <= suf) {
-        unsigned cum = above_lane;
-#pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          if (cum + h[j] >= need) {
-            sm.pick_digit = lane * 8 + j;
-            sm.pick_above = cum;
-            sm.pick_count = h[j];
-            break;
-          }
-          cum += h[j];
-        }
+    if (w == 0) pick_bin(sm, need, lane);
+    __syncthreads();
+    const unsigned bsel = static_cast<unsigned>(sm.pick_digit);
+    need -= sm.pick_above;
+    const unsigned cnt = sm.pick_count;
+    prefix |= bsel << shift;
+    mask |= dmask << shift;
+    __syncthreads();  // pick_* and hist are rewritten next
+    if (cnt == need) {
+      exact = true;  // every key with this prefix is kept
+      resolved = true;
+    } else if (shift == 0) {
+      resolved = true;  // full key known; ties at it are ranked by slot
+    } else {
+      width = min(8, shift);
+      shift -= width;
+      if (staged_once && cnt <= LCAP) break;  // finish on the short list
+    }
+  }
+
+  // ---- finish on the short list of keys sharing the current prefix ---------
+  if (!resolved) {
+    for (int q = 0; q < NCH; ++q) {
+      const int j = q * NT + t;
+      const int i = c.lo + j;
+      const uint32_t k = skey[j];
+      const bool m = (i >= c.P) && (i < c.end) && ((k & mask) == prefix);
+      const unsigned bal = __ballot_sync(FULL_MASK, m);
+      unsigned wbase = 0u;
+      if (lane == 0 && bal) wbase = atomicAdd(&sm.nlist, static_cast<unsigned>(__popc(bal)));
+      wbase = __shfl_sync(FULL_MASK, wbase, 0);
+      if (m) {
+        const unsigned at = wbase + __popc(bal & ((1u << lane) - 1u));
+        lkey[at] = k;
+        lslot[at] = i;
       }
     }
     __syncthreads();
-    const unsigned b = static_cast<unsigned>(sm.pick_digit);
-    need -= sm.pick_above;
-    const unsigned cnt = sm.pick_count;
-    prefix |= b << shift;
-    mask |= 0xffu << shift;
-    __syncthreads();  // pick_* are rewritten by the next pass
-    if (cnt == need) {
-      exact = true;  // every key with this prefix is kept
-      break;
+    const int nl = static_cast<int>(sm.nlist);
+    while (!resolved) {
+      if (t < 256) sm.hist[t] = 0u;
+      __syncthreads();
+      const uint32_t dmask = (1u << width) - 1u;
+      for (int e0 = 0; e0 < nl; e0 += NT) {  // uniform trip count: match.any needs the full warp
+        const int e = e0 + t;
+        const uint32_t k = (e < nl) ? lkey[e] : 0u;
+        const bool act = (e < nl) && ((k & mask) == prefix);
+        hist_add(sm, act, (k >> shift) & dmask, lane);
+      }
+      __syncthreads();
+      if (w == 0) pick_bin(sm, need, lane);
+      __syncthreads();
+      const unsigned bsel = static_cast<unsigned>(sm.pick_digit);
+      need -= sm.pick_above;
+      const unsigned cnt = sm.pick_count;
+      prefix |= bsel << shift;
+      mask |= dmask << shift;
+      __syncthreads();
+      if (cnt == need) {
+        exact = true;
+        resolved = true;
+      } else if (shift == 0) {
+        resolved = true;
+      } else {
+        width = min(8, shift);
+        shift -= width;
+      }
     }
   }
 
@@ -239,7 +401,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
   for (int sc = 0; sc < n_super; ++sc) {
     const int base = c.lo + sc * KCAP;
     if (!staged_once) {
-      stage_keys<RANDOM>(p, c, base, skey, nan);
+      uint32_t a = 0xffffffffu, b = 0u;
+      stage_keys<RANDOM>(p, c, base, skey, nan, a, b);
       __syncthreads();
     }
     uint32_t eqb = 0u, gtb = 0u;
@@ -286,9 +449,9 @@ cudaError_t launch_one(const SelectParams& p, int n_slices, cudaStream_t st) {
   // setting it on every call is cheap and covers every device.
   const cudaError_t e = cudaFuncSetAttribute(select_kernel<RANDOM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(KEY_SMEM));
+                                             static_cast<int>(SEL_SMEM));
   if (e != cudaSuccess) return e;
-  select_kernel<RANDOM><<<n_slices, NT, KEY_SMEM, st>>>(p);
+  select_kernel<RANDOM><<<n_slices, NT, SEL_SMEM, st>>>(p);
   note_launch();
   return cudaGetLastError();
 }
