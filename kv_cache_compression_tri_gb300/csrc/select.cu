@@ -6,19 +6,21 @@
 // [n-W, n), ascending. One CTA of 1024 threads owns one slice:
 //   1. candidate keys -- the order-preserving u32 of the fp32 score, or the
 //      Philox-4x32-10 draw -- are staged in shared memory (up to 32768,
-//      128 KB), slot-ordered, while the block finds their min and max;
-//   2. the bits above the highest bit where min and max differ are common to
-//      every key, so the first 8-bit radix digit starts just below them and
-//      spans the keys' real range; one histogram pass over all keys (shared
-//      atomics merged per digit with match.any) finds the digit bin that
-//      holds the k-th largest key;
+//      128 KB), slot-ordered; warp w owns slots [1024 w, 1024 w + 1024) and
+//      lane l reads slot 1024 w + 32 q + l at step q (conflict-free);
+//   2. the block finds the keys' min and max: bits above the highest bit
+//      where they differ are common to all keys, so the first 8-bit radix
+//      digit starts just below them and spans the keys' real range; one
+//      histogram pass (per-warp private histograms, plain shared atomics)
+//      finds the digit bin holding the k-th largest key;
 //   3. the keys of that bin (a few hundred typically) are collected into a
 //      short list and the remaining digits are resolved on the list only;
 //      the select stops as soon as a bin is taken whole;
-//   4. one block-wide scan in slot order (warp ballots plus one scan over
-//      (chunk, warp) counts) emits the keep list ascending without sorting;
-//      among keys equal to the threshold the lower slots win (ranked by a
-//      second scan only when needed).
+//   4. emission in slot order: each lane keeps one bit per step for "above
+//      the threshold" and "equal to it"; warp ballots give ranks inside a
+//      warp and a 32-entry scan of warp totals gives the warp's offset, so
+//      the keep list comes out ascending without sorting; among keys equal
+//      to the threshold the lower slots win.
 // Slices with more than 32768 candidates, or whose threshold bin does not
 // fit the list, fall back to full-array radix passes (re-staging the keys
 // for every pass when they do not fit shared memory).
@@ -31,10 +33,13 @@ namespace {
 
 constexpr int NT = 1024;
 constexpr int NW = NT / 32;
-constexpr int KCAP = 32768;     // keys staged per super-chunk
-constexpr int NCH = KCAP / NT;  // chunks of NT slots per super-chunk
-constexpr int LCAP = 4096;      // short-list capacity
-constexpr size_t SEL_SMEM = KCAP * sizeof(uint32_t) + LCAP * (sizeof(uint32_t) + sizeof(int32_t));
+constexpr int KCAP = 32768;       // keys staged per super-chunk
+constexpr int WSPAN = KCAP / NW;  // slots per warp (1024)
+constexpr int NQ = WSPAN / 32;    // steps per lane (32)
+constexpr int LCAP = 4096;        // short-list capacity
+constexpr size_t SEL_SMEM = KCAP * sizeof(uint32_t)              // keys
+                            + NW * 256 * sizeof(unsigned)         // per-warp histograms
+                            + LCAP * sizeof(uint32_t);            // short list
 
 struct SliceCtx {
   int64_t s;
@@ -46,144 +51,84 @@ struct SliceCtx {
 
 struct Smem {
   unsigned hist[256];
-  unsigned tot[NCH * NW];  // per (chunk, warp) counts, then exclusive offsets
-  unsigned wsum[NW];
+  unsigned wtot[NW];
   unsigned wmin[NW], wmax[NW];
-  unsigned total;
   int pick_digit;
   unsigned pick_above, pick_count;
   unsigned nlist;
   int nan_seen;
 };
 
+__device__ __forceinline__ bool in_range(int i, int lo, int hi) {
+  return static_cast<unsigned>(i - lo) < static_cast<unsigned>(hi - lo);
+}
+
 // Stage the keys of slots [base, base + KCAP) into skey (slot-ordered).
 // Slots outside [P, end) get key 0 and are masked out by their index later.
-// Returns this thread's min / max over the valid keys it staged.
+// Accumulates this thread's min / max over the valid keys it staged.
 template <bool RANDOM>
 __device__ __forceinline__ void stage_keys(const SelectParams& p, const SliceCtx& c, int base,
                                            uint32_t* skey, bool& nan, uint32_t& kmin, uint32_t& kmax) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int V = WSPAN / 4 / 32;  // 16-byte groups per lane (8)
   if (RANDOM) {
     // one Philox call yields the draws of 4 consecutive slots (base % 4 == 0)
     const uint2 key = make_uint2(static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
     const uint32_t lay = static_cast<uint32_t>(c.head + 65536 * c.layer);
 #pragma unroll 2
-    for (int g = threadIdx.x; g < KCAP / 4; g += NT) {
+    for (int v = 0; v < V; ++v) {
+      const int g = w * (WSPAN / 4) + v * 32 + lane;
       const int i0 = base + 4 * g;
       uint4 r = make_uint4(0u, 0u, 0u, 0u);
       if (i0 < c.end)
         r = philox4x32_10(
             make_uint4(static_cast<uint32_t>(i0) >> 2, lay, static_cast<uint32_t>(c.seq), p.round), key);
-      const uint32_t v[4] = {r.x, r.y, r.z, r.w};
+      const uint32_t e4[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool valid = (i0 + e >= c.P) && (i0 + e < c.end);
-        if (valid) {
-          kmin = min(kmin, v[e]);
-          kmax = max(kmax, v[e]);
+        if (in_range(i0 + e, c.P, c.end)) {
+          kmin = min(kmin, e4[e]);
+          kmax = max(kmax, e4[e]);
         }
       }
       reinterpret_cast<uint4*>(skey)[g] = r;
     }
   } else {
     const float* row = p.scores + c.s * static_cast<int64_t>(p.n_cap);
-    if (((c.s * static_cast<int64_t>(p.n_cap) + base) & 3) == 0) {
-      // 16-byte loads, all issued before any is used
-      constexpr int PER = KCAP / 4 / NT;
-      float4 v[PER];
+    const bool vec = ((c.s * static_cast<int64_t>(p.n_cap) + base) & 3) == 0;
+    float4 f[V];
 #pragma unroll
-      for (int q = 0; q < PER; ++q) {
-        const int i0 = base + 4 * (q * NT + threadIdx.x);
-        if (i0 + 3 < c.end) {
-          v[q] = __ldcg(reinterpret_cast<const float4*>(row + i0));
-        } else {
-          v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (i0 < c.end) v[q].x = __ldcg(row + i0);
-          if (i0 + 1 < c.end) v[q].y = __ldcg(row + i0 + 1);
-          if (i0 + 2 < c.end) v[q].z = __ldcg(row + i0 + 2);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < PER; ++q) {
-        const int i0 = base + 4 * (q * NT + threadIdx.x);
-        const float f[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-        uint32_t k[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const bool valid = (i0 + e >= c.P) && (i0 + e < c.end);
-          k[e] = valid ? score_key(f[e], nan) : 0u;
-          if (valid) {
-            kmin = min(kmin, k[e]);
-            kmax = max(kmax, k[e]);
-          }
-        }
-        reinterpret_cast<uint4*>(skey)[q * NT + threadIdx.x] = make_uint4(k[0], k[1], k[2], k[3]);
-      }
-    } else {
-      for (int j = threadIdx.x; j < KCAP; j += NT) {
-        const int i = base + j;
-        uint32_t k = 0u;
-        if (i >= c.P && i < c.end) {
-          k = score_key(__ldcg(row + i), nan);
-          kmin = min(kmin, k);
-          kmax = max(kmax, k);
-        }
-        skey[j] = k;
+    for (int v = 0; v < V; ++v) {
+      const int g = w * (WSPAN / 4) + v * 32 + lane;
+      const int i0 = base + 4 * g;
+      if (vec && i0 + 3 < c.end) {
+        f[v] = __ldcg(reinterpret_cast<const float4*>(row + i0));
+      } else {
+        f[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i0 < c.end) f[v].x = __ldcg(row + i0);
+        if (i0 + 1 < c.end) f[v].y = __ldcg(row + i0 + 1);
+        if (i0 + 2 < c.end) f[v].z = __ldcg(row + i0 + 2);
+        if (i0 + 3 < c.end) f[v].w = __ldcg(row + i0 + 3);
       }
     }
-  }
-}
-
-// Block-wide exclusive scan of sm.tot[0..count) (count <= NT), in place;
-// returns the sum of all entries. Callers sync before (entries written) and
-// may read sm.tot right after it returns.
-__device__ unsigned block_exclusive_scan(Smem& sm, int count) {
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const unsigned v = (t < count) ? sm.tot[t] : 0u;
-  unsigned incl = v;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned y = __shfl_up_sync(FULL_MASK, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sm.wsum[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    const unsigned x = sm.wsum[lane];
-    unsigned xi = x;
+    for (int v = 0; v < V; ++v) {
+      const int g = w * (WSPAN / 4) + v * 32 + lane;
+      const int i0 = base + 4 * g;
+      const float x[4] = {f[v].x, f[v].y, f[v].z, f[v].w};
+      uint32_t k[4];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned y = __shfl_up_sync(FULL_MASK, xi, o);
-      if (lane >= o) xi += y;
+      for (int e = 0; e < 4; ++e) {
+        const bool valid = in_range(i0 + e, c.P, c.end);
+        k[e] = valid ? score_key(x[e], nan) : 0u;
+        if (valid) {
+          kmin = min(kmin, k[e]);
+          kmax = max(kmax, k[e]);
+        }
+      }
+      reinterpret_cast<uint4*>(skey)[g] = make_uint4(k[0], k[1], k[2], k[3]);
     }
-    sm.wsum[lane] = xi - x;  // exclusive
-    if (lane == 31) sm.total = xi;
   }
-  __syncthreads();
-  if (t < count) sm.tot[t] = incl - v + sm.wsum[w];
-  const unsigned total = sm.total;
-  __syncthreads();
-  return total;
-}
-
-// Flags packed one bit per chunk (bit q: slot base + q*NT + threadIdx.x).
-// Writes the exclusive slot-order offset of each (chunk, warp) into
-// sm.tot[q*NW + w] and returns the total.
-__device__ __forceinline__ unsigned chunk_offsets(Smem& sm, uint32_t bits, int lane, int w) {
-#pragma unroll
-  for (int q = 0; q < NCH; ++q) {
-    const unsigned b = __ballot_sync(FULL_MASK, (bits >> q) & 1u);
-    if (lane == 0) sm.tot[q * NW + w] = __popc(b);
-  }
-  __syncthreads();
-  return block_exclusive_scan(sm, NCH * NW);
-}
-
-// Add one key to the digit histogram; lanes with the same digit are merged
-// so each distinct digit costs one shared atomic per warp.
-__device__ __forceinline__ void hist_add(Smem& sm, bool act, unsigned digit, int lane) {
-  const unsigned d = act ? digit : 256u;
-  const unsigned peers = __match_any_sync(FULL_MASK, d);
-  if (act && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], __popc(peers));
 }
 
 // Warp 0 finds digit b with count(digits > b) < need <= count(digits >= b)
@@ -217,11 +162,25 @@ __device__ __forceinline__ void pick_bin(Smem& sm, unsigned need, int lane) {
   }
 }
 
+// Exclusive prefix of this warp's entry among the 32 warp totals in
+// sm.wtot, and the grand total (every warp computes it redundantly).
+__device__ __forceinline__ unsigned warp_offset(const Smem& sm, int w, int lane, unsigned& total) {
+  const unsigned x = sm.wtot[lane];
+  unsigned incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(FULL_MASK, incl, o);
+    if (lane >= o) incl += y;
+  }
+  total = __shfl_sync(FULL_MASK, incl, 31);
+  return __shfl_sync(FULL_MASK, incl - x, w);
+}
+
 template <bool RANDOM>
 __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(16) uint32_t skey[];
-  uint32_t* lkey = skey + KCAP;
-  int32_t* lslot = reinterpret_cast<int32_t*>(lkey + LCAP);
+  unsigned* whist = skey + KCAP;  // [NW][256]
+  uint32_t* lkey = whist + NW * 256;
   __shared__ Smem sm;
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -264,6 +223,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
   int width = 8;   // bits of the next digit
   unsigned need = static_cast<unsigned>(need_total);
   bool exact = false, resolved = false;
+  const int wbase_slot = w * WSPAN + lane;  // slot offset of (warp, lane) at step 0
 
   if (staged_once) {
     uint32_t kmin = 0xffffffffu, kmax = 0u;
@@ -285,7 +245,6 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
       kmin = min(kmin, __shfl_xor_sync(FULL_MASK, kmin, o));
       kmax = max(kmax, __shfl_xor_sync(FULL_MASK, kmax, o));
     }
-    // every thread now holds the block min and max
     const uint32_t diff = kmin ^ kmax;
     if (diff == 0u) {
       prefix = kmin;  // all candidates equal: lowest slots win
@@ -301,26 +260,32 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
   }
 
   // ---- radix passes over the full key array -------------------------------
-  // (once when staged in shared memory; until resolved when streaming)
+  unsigned* my_hist = whist + w * 256;
   while (!resolved) {
-    if (t < 256) sm.hist[t] = 0u;
-    __syncthreads();
+    for (int b = lane; b < 256; b += 32) my_hist[b] = 0u;
+    __syncwarp();
     const uint32_t dmask = (1u << width) - 1u;
     for (int sc = 0; sc < n_super; ++sc) {
       const int base = c.lo + sc * KCAP;
       if (!staged_once) {
         uint32_t a = 0xffffffffu, b = 0u;
+        __syncthreads();  // previous users of skey are done
         stage_keys<RANDOM>(p, c, base, skey, nan, a, b);
         __syncthreads();
       }
-      for (int q = 0; q < NCH; ++q) {
-        const int j = q * NT + t;
-        const int i = base + j;
+#pragma unroll 8
+      for (int q = 0; q < NQ; ++q) {
+        const int j = wbase_slot + q * 32;
         const uint32_t k = skey[j];
-        const bool act = (i >= c.P) && (i < c.end) && ((k & mask) == prefix);
-        hist_add(sm, act, (k >> shift) & dmask, lane);
+        if (in_range(base + j, c.P, c.end) && (k & mask) == prefix) atomicAdd(&my_hist[(k >> shift) & dmask], 1u);
       }
-      if (!staged_once) __syncthreads();  // skey is re-staged next
+    }
+    __syncthreads();
+    if (t < 256) {
+      unsigned sum = 0u;
+#pragma unroll 8
+      for (int ww = 0; ww < NW; ++ww) sum += whist[ww * 256 + t];
+      sm.hist[t] = sum;
     }
     __syncthreads();
     if (w == 0) pick_bin(sm, need, lane);
@@ -330,7 +295,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
     const unsigned cnt = sm.pick_count;
     prefix |= bsel << shift;
     mask |= dmask << shift;
-    __syncthreads();  // pick_* and hist are rewritten next
+    __syncthreads();  // pick_* and the histograms are rewritten next
     if (cnt == need) {
       exact = true;  // every key with this prefix is kept
       resolved = true;
@@ -345,19 +310,20 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
 
   // ---- finish on the short list of keys sharing the current prefix ---------
   if (!resolved) {
-    for (int q = 0; q < NCH; ++q) {
-      const int j = q * NT + t;
-      const int i = c.lo + j;
+#pragma unroll 4
+    for (int q = 0; q < NQ; ++q) {
+      const int j = wbase_slot + q * 32;
       const uint32_t k = skey[j];
-      const bool m = (i >= c.P) && (i < c.end) && ((k & mask) == prefix);
+      const bool m = in_range(c.lo + j, c.P, c.end) && ((k & mask) == prefix);
       const unsigned bal = __ballot_sync(FULL_MASK, m);
-      unsigned wbase = 0u;
-      if (lane == 0 && bal) wbase = atomicAdd(&sm.nlist, static_cast<unsigned>(__popc(bal)));
-      wbase = __shfl_sync(FULL_MASK, wbase, 0);
-      if (m) {
-        const unsigned at = wbase + __popc(bal & ((1u << lane) - 1u));
-        lkey[at] = k;
-        lslot[at] = i;
+      if (bal) {
+        unsigned at = 0u;
+        if (lane == 0) at = atomicAdd(&sm.nlist, static_cast<unsigned>(__popc(bal)));
+        at = __shfl_sync(FULL_MASK, at, 0);
+        if (m) {
+          at += __popc(bal & ((1u << lane) - 1u));
+          lkey[at] = k;
+        }
       }
     }
     __syncthreads();
@@ -366,11 +332,9 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
       if (t < 256) sm.hist[t] = 0u;
       __syncthreads();
       const uint32_t dmask = (1u << width) - 1u;
-      for (int e0 = 0; e0 < nl; e0 += NT) {  // uniform trip count: match.any needs the full warp
-        const int e = e0 + t;
-        const uint32_t k = (e < nl) ? lkey[e] : 0u;
-        const bool act = (e < nl) && ((k & mask) == prefix);
-        hist_add(sm, act, (k >> shift) & dmask, lane);
+      for (int e = t; e < nl; e += NT) {
+        const uint32_t k = lkey[e];
+        if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
       }
       __syncthreads();
       if (w == 0) pick_bin(sm, need, lane);
@@ -402,38 +366,50 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
     const int base = c.lo + sc * KCAP;
     if (!staged_once) {
       uint32_t a = 0xffffffffu, b = 0u;
+      __syncthreads();
       stage_keys<RANDOM>(p, c, base, skey, nan, a, b);
       __syncthreads();
     }
     uint32_t eqb = 0u, gtb = 0u;
 #pragma unroll
-    for (int q = 0; q < NCH; ++q) {
-      const int j = q * NT + t;
-      const int i = base + j;
+    for (int q = 0; q < NQ; ++q) {
+      const int j = wbase_slot + q * 32;
       const uint32_t k = skey[j] & mask;
-      const bool valid = (i >= c.P) && (i < c.end);
-      if (valid && k > prefix) gtb |= 1u << q;
-      if (valid && k == prefix) eqb |= 1u << q;
+      const bool valid = in_range(base + j, c.P, c.end);
+      gtb |= static_cast<uint32_t>(valid && k > prefix) << q;
+      eqb |= static_cast<uint32_t>(valid && k == prefix) << q;
     }
     if (!exact) {
-      const unsigned total_eq = chunk_offsets(sm, eqb, lane, w);
+      unsigned cnt = 0u;
 #pragma unroll
-      for (int q = 0; q < NCH; ++q) {
+      for (int q = 0; q < NQ; ++q) cnt += __popc(__ballot_sync(FULL_MASK, (eqb >> q) & 1u));
+      if (lane == 0) sm.wtot[w] = cnt;
+      __syncthreads();
+      unsigned total_eq;
+      unsigned rank = eq_carry + warp_offset(sm, w, lane, total_eq);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
         const unsigned bq = __ballot_sync(FULL_MASK, (eqb >> q) & 1u);
-        const unsigned rank = eq_carry + sm.tot[q * NW + w] + __popc(bq & lt_mask);
-        if (((eqb >> q) & 1u) && rank >= need) eqb &= ~(1u << q);
+        if (((eqb >> q) & 1u) && rank + __popc(bq & lt_mask) >= need) eqb &= ~(1u << q);
+        rank += __popc(bq);
       }
       eq_carry += total_eq;
-      __syncthreads();  // sm.tot is rewritten below
+      __syncthreads();  // sm.wtot is rewritten below
     }
     const uint32_t kb = gtb | eqb;
-    const unsigned total_keep = chunk_offsets(sm, kb, lane, w);
+    unsigned cnt = 0u;
 #pragma unroll
-    for (int q = 0; q < NCH; ++q) {
+    for (int q = 0; q < NQ; ++q) cnt += __popc(__ballot_sync(FULL_MASK, (kb >> q) & 1u));
+    if (lane == 0) sm.wtot[w] = cnt;
+    __syncthreads();
+    unsigned total_keep;
+    unsigned rank = keep_carry + warp_offset(sm, w, lane, total_keep);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
       const unsigned bq = __ballot_sync(FULL_MASK, (kb >> q) & 1u);
-      const unsigned rank = keep_carry + sm.tot[q * NW + w] + __popc(bq & lt_mask);
-      if (((kb >> q) & 1u) && rank < static_cast<unsigned>(need_total))
-        keep[c.P + rank] = base + q * NT + t;
+      const unsigned r = rank + __popc(bq & lt_mask);
+      if (((kb >> q) & 1u) && r < static_cast<unsigned>(need_total)) keep[c.P + r] = base + wbase_slot + q * 32;
+      rank += __popc(bq);
     }
     keep_carry += total_keep;
     __syncthreads();
