@@ -1,11 +1,11 @@
 // select.cu -- per-slice budgeted top-k selection in one CTA.
 //
-// TriAttention paper summary, "Retention and eviction" (top-B by score) and
-// Random Attention, Eq. 2 / Eq. 3 / Algorithm 1 (top-K of i.i.d. uniform
-// draws, prompt forced in): keep [0, P) U top-(B-P-W) candidates U
-// [n-W, n), ascending. One CTA of 1024 threads owns one slice:
-//   1. candidate keys -- the order-preserving u32 of the fp32 score, or the
-//      Philox-4x32-10 draw -- are staged in shared memory (up to 32768,
+// TriAttention paper summary, "Retention and eviction" (top-B by score);
+// Random Attention, Eq. 2 (top-K with the prompt forced in): keep [0, P) U
+// top-(B-P-W) candidates U [n-W, n), ascending. One CTA of 1024 threads owns
+// one slice:
+//   1. candidate keys -- the order-preserving u32 of the fp32 score -- are
+//      staged in shared memory (up to 32768,
 //      128 KB), slot-ordered; warp w owns slots [1024 w, 1024 w + 1024) and
 //      lane l reads slot 1024 w + 32 q + l at step q (conflict-free);
 //   2. the block finds the keys' min and max: bits above the highest bit
@@ -23,7 +23,8 @@
 //      to the threshold the lower slots win.
 // Slices with more than 32768 candidates, or whose threshold bin does not
 // fit the list, fall back to full-array radix passes (re-staging the keys
-// for every pass when they do not fit shared memory).
+// for every pass when they do not fit shared memory). The Random Attention
+// draws have their own kernel (rand_select.cu).
 #include <cuda_runtime.h>
 
 #include "tri_internal.cuh"
@@ -66,68 +67,43 @@ __device__ __forceinline__ bool in_range(int i, int lo, int hi) {
 // Stage the keys of slots [base, base + KCAP) into skey (slot-ordered).
 // Slots outside [P, end) get key 0 and are masked out by their index later.
 // Accumulates this thread's min / max over the valid keys it staged.
-template <bool RANDOM>
 __device__ __forceinline__ void stage_keys(const SelectParams& p, const SliceCtx& c, int base,
                                            uint32_t* skey, bool& nan, uint32_t& kmin, uint32_t& kmax) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int V = WSPAN / 4 / 32;  // 16-byte groups per lane (8)
-  if (RANDOM) {
-    // one Philox call yields the draws of 4 consecutive slots (base % 4 == 0)
-    const uint2 key = make_uint2(static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
-    const uint32_t lay = static_cast<uint32_t>(c.head + 65536 * c.layer);
-#pragma unroll 2
-    for (int v = 0; v < V; ++v) {
-      const int g = w * (WSPAN / 4) + v * 32 + lane;
-      const int i0 = base + 4 * g;
-      uint4 r = make_uint4(0u, 0u, 0u, 0u);
-      if (i0 < c.end)
-        r = philox4x32_10(
-            make_uint4(static_cast<uint32_t>(i0) >> 2, lay, static_cast<uint32_t>(c.seq), p.round), key);
-      const uint32_t e4[4] = {r.x, r.y, r.z, r.w};
+  const float* row = p.scores + c.s * static_cast<int64_t>(p.n_cap);
+  const bool vec = ((c.s * static_cast<int64_t>(p.n_cap) + base) & 3) == 0;
+  float4 f[V];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (in_range(i0 + e, c.P, c.end)) {
-          kmin = min(kmin, e4[e]);
-          kmax = max(kmax, e4[e]);
-        }
-      }
-      reinterpret_cast<uint4*>(skey)[g] = r;
+  for (int v = 0; v < V; ++v) {
+    const int g = w * (WSPAN / 4) + v * 32 + lane;
+    const int i0 = base + 4 * g;
+    if (vec && i0 + 3 < c.end) {
+      f[v] = __ldcg(reinterpret_cast<const float4*>(row + i0));
+    } else {
+      f[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i0 < c.end) f[v].x = __ldcg(row + i0);
+      if (i0 + 1 < c.end) f[v].y = __ldcg(row + i0 + 1);
+      if (i0 + 2 < c.end) f[v].z = __ldcg(row + i0 + 2);
+      if (i0 + 3 < c.end) f[v].w = __ldcg(row + i0 + 3);
     }
-  } else {
-    const float* row = p.scores + c.s * static_cast<int64_t>(p.n_cap);
-    const bool vec = ((c.s * static_cast<int64_t>(p.n_cap) + base) & 3) == 0;
-    float4 f[V];
+  }
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int g = w * (WSPAN / 4) + v * 32 + lane;
-      const int i0 = base + 4 * g;
-      if (vec && i0 + 3 < c.end) {
-        f[v] = __ldcg(reinterpret_cast<const float4*>(row + i0));
-      } else {
-        f[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i0 < c.end) f[v].x = __ldcg(row + i0);
-        if (i0 + 1 < c.end) f[v].y = __ldcg(row + i0 + 1);
-        if (i0 + 2 < c.end) f[v].z = __ldcg(row + i0 + 2);
-        if (i0 + 3 < c.end) f[v].w = __ldcg(row + i0 + 3);
+  for (int v = 0; v < V; ++v) {
+    const int g = w * (WSPAN / 4) + v * 32 + lane;
+    const int i0 = base + 4 * g;
+    const float x[4] = {f[v].x, f[v].y, f[v].z, f[v].w};
+    uint32_t k[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool valid = in_range(i0 + e, c.P, c.end);
+      k[e] = valid ? score_key(x[e], nan) : 0u;
+      if (valid) {
+        kmin = min(kmin, k[e]);
+        kmax = max(kmax, k[e]);
       }
     }
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int g = w * (WSPAN / 4) + v * 32 + lane;
-      const int i0 = base + 4 * g;
-      const float x[4] = {f[v].x, f[v].y, f[v].z, f[v].w};
-      uint32_t k[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool valid = in_range(i0 + e, c.P, c.end);
-        k[e] = valid ? score_key(x[e], nan) : 0u;
-        if (valid) {
-          kmin = min(kmin, k[e]);
-          kmax = max(kmax, k[e]);
-        }
-      }
-      reinterpret_cast<uint4*>(skey)[g] = make_uint4(k[0], k[1], k[2], k[3]);
-    }
+    reinterpret_cast<uint4*>(skey)[g] = make_uint4(k[0], k[1], k[2], k[3]);
   }
 }
 
@@ -176,7 +152,6 @@ __device__ __forceinline__ unsigned warp_offset(const Smem& sm, int w, int lane,
   return __shfl_sync(FULL_MASK, incl - x, w);
 }
 
-template <bool RANDOM>
 __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(16) uint32_t skey[];
   unsigned* whist = skey + KCAP;  // [NW][256]
@@ -227,7 +202,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
 
   if (staged_once) {
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    stage_keys<RANDOM>(p, c, c.lo, skey, nan, kmin, kmax);
+    stage_keys(p, c, c.lo, skey, nan, kmin, kmax);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       kmin = min(kmin, __shfl_xor_sync(FULL_MASK, kmin, o));
@@ -270,7 +245,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
       if (!staged_once) {
         uint32_t a = 0xffffffffu, b = 0u;
         __syncthreads();  // previous users of skey are done
-        stage_keys<RANDOM>(p, c, base, skey, nan, a, b);
+        stage_keys(p, c, base, skey, nan, a, b);
         __syncthreads();
       }
 #pragma unroll 8
@@ -367,7 +342,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
     if (!staged_once) {
       uint32_t a = 0xffffffffu, b = 0u;
       __syncthreads();
-      stage_keys<RANDOM>(p, c, base, skey, nan, a, b);
+      stage_keys(p, c, base, skey, nan, a, b);
       __syncthreads();
     }
     uint32_t eqb = 0u, gtb = 0u;
@@ -419,23 +394,17 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
   if (t == 0 && sm.nan_seen) set_status(p.dev_status, TRI_DEV_NAN_SCORE);
 }
 
-template <bool RANDOM>
-cudaError_t launch_one(const SelectParams& p, int n_slices, cudaStream_t st) {
-  // The dynamic shared memory opt-in is a per-device function attribute;
-  // setting it on every call is cheap and covers every device.
-  const cudaError_t e = cudaFuncSetAttribute(select_kernel<RANDOM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(SEL_SMEM));
-  if (e != cudaSuccess) return e;
-  select_kernel<RANDOM><<<n_slices, NT, SEL_SMEM, st>>>(p);
-  note_launch();
-  return cudaGetLastError();
-}
-
 }  // namespace
 
-cudaError_t launch_select(const SelectParams& p, bool random, int n_slices, cudaStream_t st) {
-  return random ? launch_one<true>(p, n_slices, st) : launch_one<false>(p, n_slices, st);
+cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st) {
+  // The dynamic shared memory opt-in is a per-device function attribute;
+  // setting it on every call is cheap and covers every device.
+  const cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(SEL_SMEM));
+  if (e != cudaSuccess) return e;
+  select_kernel<<<n_slices, NT, SEL_SMEM, st>>>(p);
+  note_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace tri

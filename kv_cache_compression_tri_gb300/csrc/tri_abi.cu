@@ -204,7 +204,7 @@ tri_status tri_select_topk(const float* scores, const tri_kv* kv, int32_t n_prom
   p.budget = budget;
   p.n_layers = kv->n_layers;
   p.n_kv_heads = kv->n_kv_heads;
-  const cudaError_t e = launch_select(p, false, static_cast<int>(slices_of(kv)), stream);
+  const cudaError_t e = launch_select(p, static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 
@@ -229,7 +229,7 @@ tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n
   p.n_kv_heads = kv->n_kv_heads;
   p.seed = seed;
   p.round = round;
-  const cudaError_t e = launch_select(p, true, static_cast<int>(slices_of(kv)), stream);
+  const cudaError_t e = launch_rand_select(p, static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 

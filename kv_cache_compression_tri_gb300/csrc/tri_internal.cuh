@@ -250,7 +250,8 @@ struct ScoreGeometry {
   int tile_rows;
 };
 ScoreGeometry score_geometry(tri_dtype dt, int head_dim);
-cudaError_t launch_select(const SelectParams& p, bool random, int n_slices, cudaStream_t st);
+cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st);
+cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_calibrate(const CalibParams& p, tri_dtype dt, int head_dim,
                              tri_rope_style style, int lh_count, cudaStream_t st);

@@ -110,6 +110,8 @@ def scaled(w: Workload, **over) -> Workload:
 # Profiling case: the stack with one sequence (288 slices, 2.4 GB of K).
 WORKLOADS["qwen3_8b_stack_1seq"] = scaled(WORKLOADS["qwen3_8b_stack"], name="qwen3_8b_stack_1seq", n_seq=1,
                                           description="one sequence of the Qwen3-8B-shaped stack")
+WORKLOADS["random_stack_1seq"] = scaled(WORKLOADS["random_stack"], name="random_stack_1seq", n_seq=1,
+                                        description="one sequence of the Random Attention stack")
 WORKLOADS["periodic_1seq"] = scaled(WORKLOADS["periodic_large_batch"], name="periodic_1seq", n_seq=1,
                                     description="one sequence of the large-batch periodic workload")
 

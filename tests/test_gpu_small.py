@@ -330,3 +330,23 @@ def test_pipeline_against_oracle(wname):
         assert np.array_equal(kv.pos_out[s, :B].cpu().numpy(), g_keep[s])
     assert torch.all(kv.n_valid == B)
     print(f"{wname}: near-tie swaps vs oracle ranking: {total_swaps}")
+
+
+@pytest.mark.parametrize("n_cap,P,W,B,nv", [
+    (150001, 100, 10, 90000, [150001, 150000, 70000, 149999]),  # beyond one bitmap: exact fallback, pieces
+    (5000, 7, 3, 4998, [5000, 5000, 4999, 4000]),                 # keep nearly all
+    (300, 0, 0, 10, [300, 11, 10, 299]),                          # tiny candidate sets
+])
+def test_random_bit_exact_edge_shapes(n_cap, P, W, B, nv):
+    k = torch.zeros(1, 2, 2, n_cap, 64, dtype=torch.bfloat16, device="cuda")
+    kv = tri.KVCache(k, k, torch.tensor(nv, dtype=torch.int32, device="cuda"), None, None,
+                     torch.zeros(1, dtype=torch.int32, device="cuda"))
+    keep = torch.full((4, B), -9, dtype=torch.int32, device="cuda")
+    tri.rand_evict(kv, 77, 3, P, W, B, keep)
+    torch.cuda.synchronize()
+    g = keep.cpu().numpy()
+    for s in range(4):
+        layer, head = divmod(s, 2)
+        exp = orc.rand_select(77, 3, 0, layer, head, nv[s], P, W, B)
+        assert np.array_equal(g[s], exp), s
+    assert int(kv.dev_status.item()) == 0
