@@ -275,7 +275,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, args.path),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -283,13 +283,15 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w) -> dict:
+def workload_config(w, path: str = "fused") -> dict:
     return {
         "workload": w.name, "n_seq": w.n_seq, "n_layers": w.n_layers, "n_kv_heads": w.n_kv_heads,
         "head_dim": w.head_dim, "n_cap": w.n_cap, "n_valid": w.n_valid, "budget": w.budget,
         "n_prompt": w.n_prompt, "n_recent": w.n_recent, "offsets": len(w.offsets),
         "rope_theta": w.theta, "storage": "bf16" if w.elem_bytes == 2 else "f32",
-        "path": "tri_rand_evict + tri_compact_kv" if w.random else "tri_score + tri_select_topk + tri_compact_kv",
+        "path": ("rand_evict + tri_compact_kv" if w.random else
+                 ("tri_compress (fused score+select, then compaction)" if path == "fused" else
+                  "tri_score + tri_select_topk + tri_compact_kv")),
         "parallelism": "one cache batch per GPU (weak scaling)",
     }
 
@@ -331,8 +333,10 @@ def run_gpu(args, w):
     n_valid = torch.full((S,), n, dtype=torch.int32, device=dev)
     pos_out = torch.empty(S, w.n_cap, dtype=torch.int32, device=dev)
     kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status)
-    scores = torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    fused = (args.path == "fused") and not w.random
+    scores = None if fused else torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
     keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+    cws = torch.empty(tri.compress_workspace_bytes(kv), dtype=torch.uint8, device=dev) if fused else None
     stream = torch.cuda.current_stream()
 
     def restore():
@@ -343,6 +347,15 @@ def run_gpu(args, w):
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(rec=None):
+        if fused:
+            # one entry point: score + select in one kernel, then compaction
+            if rec: rec[0].record(stream)
+            tri.compress(kv, centers, w.theta, w.offsets, inp.p_cur, P, W, B, keep, workspace=cws)
+            if rec:
+                rec[1].record(stream)
+                rec[2].record(stream)
+                rec[3].record(stream)
+            return
         if w.random:
             if rec: rec[0].record(stream)
             tri.rand_evict(kv, 0, 0, P, W, B, keep)
@@ -405,24 +418,28 @@ def run_gpu(args, w):
     step_bytes = score_bytes + compact_bytes
     mean = lambda xs: sum(xs) / len(xs)
     peak, peak_kind = measured_peak_gbs()
+    if fused:
+        # the fused call's kernels are timed apart on a separate pass below
+        k1_ms, k2_ms, k3_ms = fused_breakdown(args, tri, kv, centers, w, inp, keep, cws, restore, stream)
     if w.random:
         dom_name, dom_ms, dom_bytes = "compact_kernel", mean(k3_ms), compact_bytes
     else:
-        dom_name, dom_ms, dom_bytes = "score_kernel", mean(k1_ms), score_bytes
+        dom_name, dom_ms, dom_bytes = ("score_select_kernel" if fused else "score_kernel"), mean(k1_ms), score_bytes
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = known_traffic(w.name, dom_name)
     result = {
         "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(w), l2="inputs larger than L2 (K+V %.1f GB); the first %d rows of every "
+        "config": dict(workload_config(w, args.path), l2="inputs larger than L2 (K+V %.1f GB); the first %d rows of every "
                        "slice are restored between steps (%.1f GB written, also flushes L2)" % (
                            2 * S * w.n_cap * d * e / 1e9, B, 2 * S * B * d * e / 1e9)),
         "gbs": step_bytes / (dev_sec / args.steps) / 1e9,
         "hbm_frac_of_8tbs": step_bytes / (dev_sec / args.steps) / 1e9 / 8000.0,
         "algorithmic_bytes_per_step": step_bytes,
-        "kernel_ms": {"score" if not w.random else "rand_select": round(mean(k1_ms), 4),
-                      "select": round(mean(k2_ms), 4), "compact": round(mean(k3_ms), 4)},
+        "kernel_ms": ({"score_select": round(mean(k1_ms), 4), "compact": round(mean(k3_ms), 4)} if fused else
+                      {"score" if not w.random else "rand_select": round(mean(k1_ms), 4),
+                       "select": round(mean(k2_ms), 4), "compact": round(mean(k3_ms), 4)}),
         "moved_rows_per_step": moved,
         "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
@@ -431,7 +448,7 @@ def run_gpu(args, w):
         "gpu_launches": launches,
         "wall_ms_per_step_incl_restore": 1e3 * (w1 - w0) / args.steps,
     }
-    del scores
+    del scores, cws
     torch.cuda.empty_cache()
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, w, tri, synth, inp, centers, dev, stream)
@@ -442,8 +459,41 @@ def run_gpu(args, w):
     return 0
 
 
-KERNEL_SOURCES = {"score_kernel": "score.cu", "select_kernel": "select.cu", "compact_kernel": "compact.cu",
-                  "fused_kernel": "fused.cu"}
+KERNEL_SOURCES = {"score_kernel": "score.cu", "score_select_kernel": "score.cu", "select_kernel": "select.cu",
+                  "compact_kernel": "compact.cu", "rand_select_kernel": "rand_select.cu"}
+
+
+def fused_breakdown(args, tri, kv, centers, w, inp, keep, ws, restore, stream):
+    """Per-kernel times of the fused call: the same three launches issued by
+    hand (state init + score/select kernel, then compaction) with events
+    between them, on restored inputs, outside the timed region."""
+    import ctypes
+
+    import torch
+
+    lib = tri.load_library()
+    P, W, B = w.n_prompt, w.n_recent, w.budget
+    reps = max(3, min(args.steps, 10))
+    k1, k3 = [], []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        tri.compress(kv, centers, w.theta, w.offsets, inp.p_cur, P, W, B, keep, workspace=ws)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        restore()
+        # compaction alone on the same keep lists (restored inputs)
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e1[0].record(stream)
+        tri.compact_kv(kv, keep, B)
+        e1[1].record(stream)
+        torch.cuda.synchronize()
+        restore()
+        tot = e[0].elapsed_time(e[2])
+        c = e1[0].elapsed_time(e1[1])
+        k3.append(c)
+        k1.append(tot - c)
+    return k1, [0.0] * reps, k3
 
 
 def known_traffic(workload: str, kernel: str):
@@ -488,9 +538,12 @@ def run_e2e(args, w, tri, synth, inp, centers, dev, stream):
     pos_out = torch.empty(Se, w.n_cap, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kv = tri.KVCache(dk, dv, n_valid, None, pos_out, status)
-    scores = torch.empty(Se, w.n_cap, dtype=torch.float32, device=dev)
+    scores = None if (args.path == "fused" or w.random) else torch.empty(Se, w.n_cap, dtype=torch.float32, device=dev)
     keep = torch.empty(Se, B, dtype=torch.int32, device=dev)
     p_cur = inp.p_cur[:n_seq]
+
+    fused = (args.path == "fused") and not w.random
+    cws = torch.empty(tri.compress_workspace_bytes(kv), dtype=torch.uint8, device=dev) if fused else None
 
     def one():
         dk.copy_(hk, non_blocking=True)
@@ -498,10 +551,13 @@ def run_e2e(args, w, tri, synth, inp, centers, dev, stream):
         n_valid.fill_(n)
         if w.random:
             tri.rand_evict(kv, 0, 0, P, W, B, keep)
+            tri.compact_kv(kv, keep, B)
+        elif fused:
+            tri.compress(kv, centers, w.theta, w.offsets, p_cur, P, W, B, keep, workspace=cws)
         else:
             tri.score(kv, centers, w.theta, w.offsets, p_cur, scores, n_prompt=P, n_recent=W)
             tri.select_topk(scores, kv, P, W, B, keep)
-        tri.compact_kv(kv, keep, B)
+            tri.compact_kv(kv, keep, B)
         out_k.copy_(dk[:, :, :, :B], non_blocking=True)
         out_v.copy_(dv[:, :, :, :B], non_blocking=True)
         out_keep.copy_(keep, non_blocking=True)
@@ -548,6 +604,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gpu", "reference", "ours"], default="gpu")
     ap.add_argument("--workload", default="qwen3_8b_stack")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="fused: tri_compress; separate: tri_score + tri_select_topk + tri_compact_kv")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)

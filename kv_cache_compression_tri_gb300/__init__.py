@@ -21,6 +21,7 @@ from ._build import LIB as _LIB_PATH
 __all__ = [
     "TriError", "KVCache", "Centers", "lib_path", "load_library", "calibrate_centers",
     "calibrate_workspace_bytes", "score", "select_topk", "compact_kv", "rand_evict",
+    "compress", "compress_workspace_bytes",
     "launch_count", "ROPE_INTERLEAVED", "ROPE_HALF", "NORM_WEIGHTED", "NORM_UNWEIGHTED",
     "DEV_OK", "DEV_NVALID_OVER_CAP", "DEV_NAN_SCORE", "DEV_BAD_KEEP",
 ]
@@ -93,6 +94,11 @@ def load_library():
         lib.tri_compact_kv.restype = ctypes.c_int
         lib.rand_evict.argtypes = [kvp, u64, u32, i32, i32, i32, vp, vp]
         lib.rand_evict.restype = ctypes.c_int
+        lib.tri_compress_workspace_bytes.argtypes = [kvp]
+        lib.tri_compress_workspace_bytes.restype = ctypes.c_size_t
+        lib.tri_compress.argtypes = [kvp, ctypes.POINTER(_TriCenters), ctypes.c_double, ctypes.c_int,
+                                     ctypes.c_int, vp, i32, vp, i32, i32, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.tri_compress.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -246,3 +252,29 @@ def compact_kv(kv: KVCache, keep: torch.Tensor, budget: int, stream=None) -> Non
     kvs = kv._abi()
     _check("tri_compact_kv", lib.tri_compact_kv(ctypes.byref(kvs), keep.data_ptr(), budget,
                                                 _stream(stream)))
+
+
+def compress_workspace_bytes(kv: KVCache) -> int:
+    kvs = kv._abi()
+    return int(load_library().tri_compress_workspace_bytes(ctypes.byref(kvs)))
+
+
+def compress(kv: KVCache, centers: Centers, rope_theta: float, offsets, p_cur: torch.Tensor,
+             n_prompt: int, n_recent: int, budget: int, keep: torch.Tensor,
+             workspace: torch.Tensor | None = None, style: int = ROPE_INTERLEAVED,
+             norm_mode: int = NORM_WEIGHTED, stream=None) -> torch.Tensor:
+    """One compression event: score + select + compact (tri_compress)."""
+    lib = load_library()
+    offs = (ctypes.c_int32 * len(offsets))(*[int(o) for o in offsets])
+    assert p_cur.dtype == torch.int64 and p_cur.is_cuda
+    assert keep.dtype == torch.int32 and keep.is_contiguous() and keep.numel() == kv.n_slices * budget
+    kvs, cs = kv._abi(), centers._abi()
+    need = int(lib.tri_compress_workspace_bytes(ctypes.byref(kvs)))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=kv.k.device)
+    assert workspace.numel() >= need
+    _check("tri_compress", lib.tri_compress(ctypes.byref(kvs), ctypes.byref(cs), float(rope_theta), style,
+                                            norm_mode, ctypes.cast(offs, ctypes.c_void_p), len(offsets),
+                                            p_cur.data_ptr(), n_prompt, n_recent, budget, keep.data_ptr(),
+                                            workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return keep

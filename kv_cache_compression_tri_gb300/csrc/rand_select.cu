@@ -22,7 +22,7 @@
 //   3. emission from bitmaps of "above" and "equal" slots in slot order
 //      (per-thread popcounts and one block scan), the equal ones ranked by
 //      slot, so the keep list is ascending without sorting.
-// Shared memory stays small (bitmaps for 65536 slots + the list), so two
+// Shared memory stays small (bitmaps for 65536 slots + the list), so three
 // CTAs share an SM and their phases overlap. Slices with more candidates
 // than the bitmaps cover are emitted in bitmap-sized pieces.
 #include <cuda_runtime.h>
@@ -163,7 +163,7 @@ __device__ unsigned radix_step(RSmem& sm, const RCtx& c, bool from_list, int nl,
   return cnt;
 }
 
-__global__ void __launch_bounds__(RT, 2) rand_select_kernel(const __grid_constant__ SelectParams p) {
+__global__ void __launch_bounds__(RT, 3) rand_select_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(16) unsigned char rsmem_raw[];
   RSmem& sm = *reinterpret_cast<RSmem*>(rsmem_raw);
   const int t = threadIdx.x, lane = t & 31;
@@ -219,20 +219,33 @@ __global__ void __launch_bounds__(RT, 2) rand_select_kernel(const __grid_constan
     __syncthreads();
     const uint32_t t_lo = sm.t_lo, t_hi = sm.t_hi;
     unsigned hi = 0u;
+    const uint32_t win = t_hi - t_lo;
     for (int i0 = c.lo + 4 * t; i0 < c.end; i0 += 4 * RT) {
       const uint4 r = draws(c, i0);
       const uint32_t u[4] = {r.x, r.y, r.z, r.w};
-      uint32_t nib = 0u;
+      uint32_t valid = 0xfu;  // only the first and last groups hold non-candidates
+      if (i0 < c.P || i0 + 3 >= c.end) {
+        valid = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) valid |= static_cast<uint32_t>(in_range(i0 + e, c.P, c.end)) << e;
+      }
+      uint32_t nib = 0u, mid = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (!in_range(i0 + e, c.P, c.end)) continue;
-        if (u[e] > t_hi) {
-          nib |= 1u << e;
-        } else if (u[e] >= t_lo) {
-          const unsigned at = atomicAdd(&sm.nlist, 1u);
-          if (at < RLCAP) {
-            sm.lkey[at] = u[e];
-            sm.lslot[at] = i0 + e;
+        nib |= static_cast<uint32_t>(u[e] > t_hi) << e;
+        mid |= static_cast<uint32_t>(u[e] - t_lo <= win) << e;
+      }
+      nib &= valid;
+      mid &= valid & ~nib;
+      if (mid) {  // rare: a draw inside the window joins the short list
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if ((mid >> e) & 1u) {
+            const unsigned at = atomicAdd(&sm.nlist, 1u);
+            if (at < RLCAP) {
+              sm.lkey[at] = u[e];
+              sm.lslot[at] = i0 + e;
+            }
           }
         }
       }

@@ -123,11 +123,18 @@ tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layer
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 
-tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
-                     tri_rope_style style, tri_norm_mode norm_mode, const int32_t* offsets,
-                     int32_t n_offsets, const int64_t* p_cur, int32_t n_prompt,
-                     int32_t n_recent, float* scores, tri_stream_t stream) {
-  tri_status st = check_kv(kv, false);
+}  // extern "C"
+
+namespace tri {
+namespace {
+
+// Shared by tri_score and tri_compress: argument checks and the score
+// kernel's parameter block (host fp64 per-band constants).
+tri_status prepare_score(const tri_kv* kv, const tri_centers* c, double rope_theta, tri_rope_style style,
+                         tri_norm_mode norm_mode, const int32_t* offsets, int32_t n_offsets,
+                         const int64_t* p_cur, int32_t n_prompt, int32_t n_recent, float* scores,
+                         bool need_v, ScoreParams& p) {
+  tri_status st = check_kv(kv, need_v);
   if (st != TRI_OK) return st;
   if (!c || !c->center || !c->mean_norm || !c->mrl || !aligned(c->center, 8)) return TRI_ERR_INVALID_ARG;
   if (style != TRI_ROPE_INTERLEAVED && style != TRI_ROPE_HALF) return TRI_ERR_INVALID_ARG;
@@ -137,7 +144,7 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
   if (!p_cur || !aligned(p_cur, 8) || !scores || !aligned(scores, 4)) return TRI_ERR_INVALID_ARG;
   if (n_prompt < 0 || n_recent < 0) return TRI_ERR_INVALID_ARG;
 
-  ScoreParams p{};
+  p = ScoreParams{};
   const int D = kv->head_dim, F = D / 2;
   const ScoreGeometry g = score_geometry(kv->dtype, D);
   for (int f = 0; f < F; ++f) {
@@ -176,10 +183,75 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
   if (cap_rows < rpc) rpc = cap_rows;
   p.rows_per_cta = rpc;
   p.tiles_per_slice = static_cast<int32_t>((kv->n_cap + rpc - 1) / rpc);
-  const int64_t grid = slices_of(kv) * p.tiles_per_slice;
-  if (grid > 0x7fffffff) return TRI_ERR_INVALID_ARG;
-  const cudaError_t e = launch_score(p, kv->dtype, D, style, kv->pos != nullptr,
+  if (slices_of(kv) * p.tiles_per_slice > 0x7fffffff) return TRI_ERR_INVALID_ARG;
+  return TRI_OK;
+}
+
+CompactParams compact_params(const tri_kv* kv, const int32_t* keep_idx, int32_t budget) {
+  CompactParams p{};
+  p.k = static_cast<char*>(kv->k);
+  p.v = static_cast<char*>(kv->v);
+  p.pos = kv->pos;
+  p.pos_out = kv->pos_out;
+  p.n_valid = kv->n_valid;
+  p.keep = keep_idx;
+  p.dev_status = kv->dev_status;
+  p.slice_bytes = kv->slice_stride * elem_bytes(kv->dtype);
+  p.n_cap = kv->n_cap;
+  p.budget = budget;
+  p.row_bytes = kv->head_dim * elem_bytes(kv->dtype);
+  return p;
+}
+
+size_t compress_state_offset(const tri_kv* kv) {
+  const size_t scores = static_cast<size_t>(slices_of(kv)) * kv->n_cap * sizeof(float);
+  return (scores + 255) / 256 * 256;
+}
+
+}  // namespace
+}  // namespace tri
+
+extern "C" {
+
+tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
+                     tri_rope_style style, tri_norm_mode norm_mode, const int32_t* offsets,
+                     int32_t n_offsets, const int64_t* p_cur, int32_t n_prompt,
+                     int32_t n_recent, float* scores, tri_stream_t stream) {
+  ScoreParams p;
+  const tri_status st = prepare_score(kv, c, rope_theta, style, norm_mode, offsets, n_offsets, p_cur,
+                                      n_prompt, n_recent, scores, false, p);
+  if (st != TRI_OK) return st;
+  const cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, kv->pos != nullptr,
                                      static_cast<int>(slices_of(kv)), stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+size_t tri_compress_workspace_bytes(const tri_kv* kv) {
+  if (check_kv(kv, false) != TRI_OK) return 0;
+  return compress_state_offset(kv) + static_cast<size_t>(slices_of(kv)) * 3 * sizeof(uint32_t);
+}
+
+tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_theta, tri_rope_style style,
+                        tri_norm_mode norm_mode, const int32_t* offsets, int32_t n_offsets,
+                        const int64_t* p_cur, int32_t n_prompt, int32_t n_recent, int32_t budget,
+                        int32_t* keep_idx, void* ws, size_t ws_bytes, tri_stream_t stream) {
+  if (!kv) return TRI_ERR_INVALID_ARG;
+  const size_t need = tri_compress_workspace_bytes(kv);
+  if (need == 0 || ws_bytes < need || !ws || !aligned(ws, 16)) return TRI_ERR_INVALID_ARG;
+  if (!kv->pos_out || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
+  tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
+  ScoreParams p;
+  st = prepare_score(kv, c, rope_theta, style, norm_mode, offsets, n_offsets, p_cur, n_prompt, n_recent,
+                     static_cast<float*>(ws), true, p);
+  if (st != TRI_OK) return st;
+  p.state = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + compress_state_offset(kv));
+  p.keep = keep_idx;
+  p.budget = budget;
+  cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, kv->pos != nullptr,
+                               static_cast<int>(slices_of(kv)), stream, true);
+  if (e != cudaSuccess) return TRI_ERR_CUDA;
+  e = launch_compact(compact_params(kv, keep_idx, budget), static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 
@@ -239,19 +311,7 @@ tri_status tri_compact_kv(const tri_kv* kv, const int32_t* keep_idx, int32_t bud
   if (st != TRI_OK) return st;
   if (!kv->pos_out) return TRI_ERR_INVALID_ARG;
   if (!keep_idx || !aligned(keep_idx, 4) || budget < 1 || budget > kv->n_cap) return TRI_ERR_INVALID_ARG;
-  CompactParams p{};
-  p.k = static_cast<char*>(kv->k);
-  p.v = static_cast<char*>(kv->v);
-  p.pos = kv->pos;
-  p.pos_out = kv->pos_out;
-  p.n_valid = kv->n_valid;
-  p.keep = keep_idx;
-  p.dev_status = kv->dev_status;
-  p.slice_bytes = kv->slice_stride * elem_bytes(kv->dtype);
-  p.n_cap = kv->n_cap;
-  p.budget = budget;
-  p.row_bytes = kv->head_dim * elem_bytes(kv->dtype);
-  const cudaError_t e = launch_compact(p, static_cast<int>(slices_of(kv)), stream);
+  const cudaError_t e = launch_compact(compact_params(kv, keep_idx, budget), static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 

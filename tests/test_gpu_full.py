@@ -228,3 +228,59 @@ def test_periodic_large_batch_full_size():
             assert np.array_equal(pos[s, :B].cpu().numpy(), x["pos"][:B]), (rnd, s)
         assert torch.all(kv.n_valid == B)
     print(f"periodic: worst score error/M {worst:.2e}, near-tie swaps {total_swaps} over {w.rounds + 1} events")
+
+
+def test_qwen3_stack_full_size_compress():
+    """The fused entry point at full size: keep lists follow the oracle on
+    sampled slices (exactly, on the fp32 scores it left in its workspace, and
+    by the near-tie rule against fp64 scores) and the structural invariants
+    hold for every slice."""
+    w = synth.WORKLOADS["qwen3_8b_stack"]
+    S, n_cap, n, P, W, B = w.n_slices, w.n_cap, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    inp = synth.make_inputs(w, "cuda")
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    sample = synth.sample_slices(S, 24)
+    pk = {s: slice_rows(inp.k, s).cpu() for s in sample}
+    pv = {s: slice_rows(inp.v, s).cpu() for s in sample}
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv = tri.KVCache(inp.k, inp.v, inp.n_valid.clone(), None,
+                     torch.empty(S, n_cap, dtype=torch.int32, device="cuda"), status)
+    keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(tri.compress_workspace_bytes(kv), dtype=torch.uint8, device="cuda")
+    tri.compress(kv, c, w.theta, w.offsets, inp.p_cur, P, W, B, keep, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    keep_all = keep.cpu().numpy()
+    _structural(keep_all, n, P, W, B)
+    assert torch.all(kv.n_valid == B)
+    fs = ws[: S * n_cap * 4].view(torch.float32).view(S, n_cap)
+    gc, gm, gR = f64(c.center), f64(c.mean_norm), f64(c.mrl)
+    gs = {s: fs[s].cpu().numpy() for s in sample}
+
+    def check(s):
+        seq, lh = seq_lh(inp, s)
+        k64 = pk[s].to(torch.float64).numpy()
+        sref = np.zeros(n)
+        sref[P:n - W] = orc.score_series(k64[P:n - W], gc[lh], gm[lh], gR[lh], w.offsets, int(inp.p_cur[seq]),
+                                         w.theta, pos=np.arange(P, n - W))
+        M = orc.score_bound(k64, gm[lh])
+        err = float((np.abs(gs[s][P:n - W] - sref[P:n - W]) / M[P:n - W]).max())
+        problems, _ = near_tie_violations(keep_all[s], sref, M, n, P, W, B)
+        sc = gs[s].astype(np.float64)
+        sc[:P] = 0.0
+        sc[n - W:] = 0.0
+        exact = np.array_equal(keep_all[s], orc.select(sc, n, P, W, B))
+        kb, vb = _rows_bytes(pk[s]).copy(), _rows_bytes(pv[s]).copy()
+        orc.compact(kb, keep_all[s])
+        orc.compact(vb, keep_all[s])
+        same = (np.array_equal(_rows_bytes(slice_rows(inp.k, s)[:B].cpu()), kb[:B])
+                and np.array_equal(_rows_bytes(slice_rows(inp.v, s)[:B].cpu()), vb[:B]))
+        return err, problems, exact, same
+
+    res = pmap(check, sample)
+    for s, r in zip(sample, res):
+        assert r[0] <= SCORE_TOL, (s, r[0])
+        assert not r[1], (s, r[1])
+        assert r[2], s
+        assert r[3], s

@@ -350,3 +350,73 @@ def test_random_bit_exact_edge_shapes(n_cap, P, W, B, nv):
         exp = orc.rand_select(77, 3, 0, layer, head, nv[s], P, W, B)
         assert np.array_equal(g[s], exp), s
     assert int(kv.dev_status.item()) == 0
+
+
+def _compress_vs_separate(w, ragged=False, explicit_pos=False, seed=0, style=0):
+    """tri_compress must equal tri_score + tri_select_topk + tri_compact_kv."""
+    inp = synth.make_inputs(w, "cuda")
+    S, n_cap, P, W, B = w.n_slices, w.n_cap, w.n_prompt, w.n_recent, w.budget
+    rng = np.random.default_rng(seed)
+    if ragged:
+        nv = rng.integers(0, n_cap + 1, size=S)
+        nv[0], nv[-1] = n_cap, B
+        inp.n_valid = torch.tensor(nv, dtype=torch.int32, device="cuda")
+    pos = None
+    if explicit_pos:
+        pos_np = np.stack([np.sort(rng.choice(3 * n_cap, size=n_cap, replace=False)) for _ in range(S)])
+        pos = torch.tensor(pos_np, dtype=torch.int32, device="cuda")
+        inp.p_cur = torch.full((w.n_seq,), 3 * n_cap + 1, dtype=torch.int64, device="cuda")
+    c = tri.calibrate_centers(inp.q, w.group, style=style)
+    k0, v0 = inp.k.clone(), inp.v.clone()
+    # separate calls on a copy
+    kv_a = tri.KVCache(k0.clone(), v0.clone(), inp.n_valid.clone(), None if pos is None else pos.clone(),
+                       torch.zeros(S, n_cap, dtype=torch.int32, device="cuda"),
+                       torch.zeros(1, dtype=torch.int32, device="cuda"))
+    if pos is not None:
+        kv_a.pos_out = kv_a.pos
+    sc = torch.zeros(S, n_cap, device="cuda")
+    keep_a = torch.full((S, B), -5, dtype=torch.int32, device="cuda")
+    tri.score(kv_a, c, w.theta, w.offsets, inp.p_cur, sc, n_prompt=P, n_recent=W, style=style)
+    tri.select_topk(sc, kv_a, P, W, B, keep_a)
+    tri.compact_kv(kv_a, keep_a, B)
+    # fused
+    kv_b = tri.KVCache(k0.clone(), v0.clone(), inp.n_valid.clone(), None if pos is None else pos.clone(),
+                       torch.zeros(S, n_cap, dtype=torch.int32, device="cuda"),
+                       torch.zeros(1, dtype=torch.int32, device="cuda"))
+    if pos is not None:
+        kv_b.pos_out = kv_b.pos
+    keep_b = torch.full((S, B), -5, dtype=torch.int32, device="cuda")
+    ws = torch.empty(tri.compress_workspace_bytes(kv_b), dtype=torch.uint8, device="cuda")
+    n0 = tri.launch_count()
+    tri.compress(kv_b, c, w.theta, w.offsets, inp.p_cur, P, W, B, keep_b, workspace=ws, style=style)
+    torch.cuda.synchronize()
+    assert tri.launch_count() - n0 == 3  # state init, score+select, compaction
+    assert int(kv_a.dev_status.item()) == 0 and int(kv_b.dev_status.item()) == 0
+    assert torch.equal(keep_a, keep_b)
+    assert torch.equal(kv_a.k, kv_b.k) and torch.equal(kv_a.v, kv_b.v)
+    assert torch.equal(kv_a.n_valid, kv_b.n_valid)
+    nk = kv_a.n_valid.cpu().numpy()
+    for s in range(S):
+        assert torch.equal(kv_a.pos_out[s, :nk[s]], kv_b.pos_out[s, :nk[s]])
+    # the fused scores left in the workspace are the separate call's scores
+    fs = ws[: S * n_cap * 4].view(torch.float32).view(S, n_cap)
+    nv_h = inp.n_valid.cpu().numpy()
+    for s in range(S):
+        lo, hi = P, int(nv_h[s]) - W
+        if hi > lo:
+            assert torch.equal(fs[s, lo:hi], sc[s, lo:hi])
+
+
+@pytest.mark.parametrize("wname", ["tiny", "qwen3_8b_layer"])
+def test_compress_equals_separate_calls(wname):
+    _compress_vs_separate(synth.WORKLOADS[wname])
+
+
+def test_compress_ragged_explicit_positions_and_styles():
+    w = synth.scaled(LAYER, n_seq=2, n_layers=3, n_kv_heads=4, n_cap=5000, n_valid=5000, budget=1500,
+                     n_prompt=100, n_recent=50, n_cal=512)
+    _compress_vs_separate(w, ragged=True, seed=1)
+    _compress_vs_separate(w, explicit_pos=True, seed=2, style=1)
+    w2 = synth.scaled(TINY, dtype=torch.bfloat16, n_kv_heads=6, n_cap=3000, n_valid=3000, budget=700,
+                      n_prompt=0, n_recent=0)
+    _compress_vs_separate(w2, ragged=True, seed=3)
