@@ -10,8 +10,10 @@
 // min / max the scoring CTAs accumulated; a histogram sweep (per-warp
 // private histograms) picks the bin of the first digit below them; the keys
 // of that bin go to a short list on which the remaining digits are resolved;
-// an emission sweep ranks kept slots with warp ballots (flags held in
-// registers, 32 slots per lane per piece) and writes the keep list in order.
+// an emission sweep flags kept slots and writes the keep list in order.
+// Every sweep reads 16-byte groups of 4 slots, 8 groups in flight per thread
+// (one "piece" of BS*32 slots per round), so the L2 latency is paid once per
+// piece rather than once per key.
 #pragma once
 
 #include "tri_internal.cuh"
@@ -29,6 +31,7 @@ struct BlockSelectSmem {
 };
 constexpr int BSEL_LCAP = 6144;  // short-list capacity (keys)
 constexpr size_t BSEL_SMEM_BYTES = sizeof(BlockSelectSmem) + BSEL_LCAP * sizeof(uint32_t);
+constexpr int BSEL_G = 8;  // 16-byte groups per thread per piece
 
 template <int BS>
 __device__ __forceinline__ unsigned bsel_scan_warps(BlockSelectSmem& sm, int w, int lane, unsigned& total) {
@@ -73,15 +76,45 @@ __device__ __forceinline__ void bsel_pick(BlockSelectSmem& sm, unsigned need, in
   }
 }
 
+// Load the keys of one piece: thread (w, lane) gets groups
+// g = w*32*BSEL_G + j*32 + lane (j < BSEL_G), slots lo + 4g .. lo + 4g + 3;
+// slots outside [P, end) come back invalid. row is 16-byte aligned at lo.
+template <int BS>
+__device__ __forceinline__ void bsel_load_piece(const float* row, int lo, int piece, int P, int end,
+                                                uint32_t (&k)[BSEL_G][4], uint32_t (&valid)[BSEL_G],
+                                                bool& nan) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float4 f[BSEL_G];
+#pragma unroll
+  for (int j = 0; j < BSEL_G; ++j) {
+    const int i0 = lo + 4 * (piece * BS * BSEL_G + w * 32 * BSEL_G + j * 32 + lane);
+    f[j] = (i0 < end) ? __ldcg(reinterpret_cast<const float4*>(row + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int j = 0; j < BSEL_G; ++j) {
+    const int i0 = lo + 4 * (piece * BS * BSEL_G + w * 32 * BSEL_G + j * 32 + lane);
+    const float x[4] = {f[j].x, f[j].y, f[j].z, f[j].w};
+    uint32_t v = 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool ok = static_cast<unsigned>(i0 + e - P) < static_cast<unsigned>(end - P);
+      k[j][e] = ok ? score_key(x[e], nan) : 0u;
+      v |= static_cast<uint32_t>(ok) << e;
+    }
+    valid[j] = v;
+  }
+}
+
 // Select for one slice. row: the slice's scores (global, already written and
-// made visible); kmin / kmax: min and max score key over the candidates.
-// scratch: >= BSEL_SMEM_BYTES of shared memory. Must be called by all BS
-// threads of the CTA.
+// made visible; 16-byte aligned); kmin / kmax: min and max score key over the
+// candidates. scratch: >= BSEL_SMEM_BYTES of shared memory. Must be called by
+// all BS threads of the CTA.
 template <int BS>
 __device__ void block_select(const float* row, int n, int P, int W, int B, uint32_t kmin, uint32_t kmax,
                              int32_t* keep, unsigned char* scratch, int32_t* dev_status) {
   static_assert(BS % 32 == 0 && BS <= 256, "block size");
   constexpr int NWB = BS / 32;
+  constexpr int PIECE = BS * BSEL_G * 4;  // slots per piece
   BlockSelectSmem& sm = *reinterpret_cast<BlockSelectSmem*>(scratch);
   uint32_t* lkey = reinterpret_cast<uint32_t*>(scratch + sizeof(BlockSelectSmem));
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -100,7 +133,9 @@ __device__ void block_select(const float* row, int n, int P, int W, int B, uint3
     sm.nan_seen = 0;
   }
   bool nan = false;
-  auto key_at = [&](int i) -> uint32_t { return score_key(__ldcg(row + i), nan); };
+  const int lo = P & ~3;
+  const int n_pieces = (end - lo + PIECE - 1) / PIECE;
+  uint32_t k[BSEL_G][4], valid[BSEL_G];
 
   uint32_t prefix = 0u, mask = 0u;
   unsigned need = static_cast<unsigned>(need_total);
@@ -125,10 +160,14 @@ __device__ void block_select(const float* row, int n, int P, int W, int B, uint3
     for (int b = lane; b < 256; b += 32) sm.whist[w][b] = 0u;
     __syncwarp();
     const uint32_t dmask = (1u << width) - 1u;
-#pragma unroll 4
-    for (int i = P + t; i < end; i += BS) {
-      const uint32_t k = key_at(i);
-      if ((k & mask) == prefix) atomicAdd(&sm.whist[w][(k >> shift) & dmask], 1u);
+    for (int pc = 0; pc < n_pieces; ++pc) {
+      bsel_load_piece<BS>(row, lo, pc, P, end, k, valid, nan);
+#pragma unroll
+      for (int j = 0; j < BSEL_G; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (((valid[j] >> e) & 1u) && (k[j][e] & mask) == prefix)
+            atomicAdd(&sm.whist[w][(k[j][e] >> shift) & dmask], 1u);
     }
     __syncthreads();
     for (int b = t; b < 256; b += BS) {
@@ -159,28 +198,26 @@ __device__ void block_select(const float* row, int n, int P, int W, int B, uint3
 
   // ---- finish on the short list -------------------------------------------
   if (!resolved) {
-    for (int i0 = P; i0 < end; i0 += BS) {  // uniform trip count (ballot)
-      const int i = i0 + t;
-      const uint32_t k = (i < end) ? key_at(i) : 0u;
-      const bool m = (i < end) && ((k & mask) == prefix);
-      const unsigned bal = __ballot_sync(FULL_MASK, m);
-      if (bal) {
-        unsigned at = 0u;
-        if (lane == 0) at = atomicAdd(&sm.nlist, static_cast<unsigned>(__popc(bal)));
-        at = __shfl_sync(FULL_MASK, at, 0);
-        if (m) lkey[at + __popc(bal & ((1u << lane) - 1u))] = k;
-      }
+    for (int pc = 0; pc < n_pieces; ++pc) {
+      bsel_load_piece<BS>(row, lo, pc, P, end, k, valid, nan);
+#pragma unroll
+      for (int j = 0; j < BSEL_G; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (((valid[j] >> e) & 1u) && (k[j][e] & mask) == prefix) {
+            const unsigned at = atomicAdd(&sm.nlist, 1u);
+            if (at < static_cast<unsigned>(BSEL_LCAP)) lkey[at] = k[j][e];
+          }
     }
     __syncthreads();
-    const int nl = static_cast<int>(sm.nlist);
+    const int nl = min(static_cast<int>(sm.nlist), BSEL_LCAP);
     while (!resolved) {
-      if (t < 256) sm.hist[t] = 0u;
-      for (int b = t + BS; b < 256; b += BS) sm.hist[b] = 0u;
+      for (int b = t; b < 256; b += BS) sm.hist[b] = 0u;
       __syncthreads();
       const uint32_t dmask = (1u << width) - 1u;
       for (int e = t; e < nl; e += BS) {
-        const uint32_t k = lkey[e];
-        if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & dmask], 1u);
+        const uint32_t kk = lkey[e];
+        if ((kk & mask) == prefix) atomicAdd(&sm.hist[(kk >> shift) & dmask], 1u);
       }
       __syncthreads();
       if (w == 0) bsel_pick(sm, need, lane);
@@ -202,53 +239,86 @@ __device__ void block_select(const float* row, int n, int P, int W, int B, uint3
     }
   }
 
-  // ---- emission: pieces of BS*32 slots; warp w takes 32 steps of 32 --------
-  const unsigned lt_mask = (1u << lane) - 1u;
-  constexpr int PIECE = BS * 32;
+  // ---- emission, piece by piece, in slot order ------------------------------
+  // Within a piece, warp w owns groups [w*32*G, (w+1)*32*G) in slot order
+  // (group j*32 + lane is slot-ordered by (j, lane)); each lane holds a
+  // 4-bit flag nibble per group.
   unsigned eq_carry = 0u, out = 0u;
-  for (int base = P; base < end; base += PIECE) {
-    const int wb = base + w * 1024;
-    uint32_t gtb = 0u, eqb = 0u;
-#pragma unroll 8
-    for (int q = 0; q < 32; ++q) {
-      const int i = wb + q * 32 + lane;
-      if (i < end) {
-        const uint32_t k = key_at(i) & mask;
-        gtb |= static_cast<uint32_t>(k > prefix) << q;
-        eqb |= static_cast<uint32_t>(k == prefix) << q;
+  for (int pc = 0; pc < n_pieces; ++pc) {
+    bsel_load_piece<BS>(row, lo, pc, P, end, k, valid, nan);
+    uint32_t gt[BSEL_G], eq[BSEL_G];
+#pragma unroll
+    for (int j = 0; j < BSEL_G; ++j) {
+      gt[j] = eq[j] = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t km = k[j][e] & mask;
+        const uint32_t v = (valid[j] >> e) & 1u;
+        gt[j] |= (v & static_cast<uint32_t>(km > prefix)) << e;
+        eq[j] |= (v & static_cast<uint32_t>(km == prefix)) << e;
       }
     }
     if (!exact) {
       unsigned cnt = 0u;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) cnt += __popc(__ballot_sync(FULL_MASK, (eqb >> q) & 1u));
+      for (int j = 0; j < BSEL_G; ++j) cnt += __popc(eq[j]);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) cnt += __shfl_xor_sync(FULL_MASK, cnt, o);
       if (lane == 0) sm.wtot[w] = cnt;
       __syncthreads();
       unsigned tot;
       unsigned r = eq_carry + bsel_scan_warps<BS>(sm, w, lane, tot);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const unsigned bq = __ballot_sync(FULL_MASK, (eqb >> q) & 1u);
-        if (((eqb >> q) & 1u) && r + __popc(bq & lt_mask) >= need) eqb &= ~(1u << q);
-        r += __popc(bq);
+      for (int j = 0; j < BSEL_G; ++j) {
+        const unsigned c = __popc(eq[j]);
+        unsigned incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(FULL_MASK, incl, o);
+          if (lane >= o) incl += y;
+        }
+        unsigned rr = r + incl - c;
+        uint32_t kept = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((eq[j] >> e) & 1u) {
+            if (rr < need) kept |= 1u << e;
+            ++rr;
+          }
+        eq[j] = kept;
+        r += __shfl_sync(FULL_MASK, incl, 31);
       }
       eq_carry += tot;
       __syncthreads();
     }
-    const uint32_t kb = gtb | eqb;
     unsigned cnt = 0u;
 #pragma unroll
-    for (int q = 0; q < 32; ++q) cnt += __popc(__ballot_sync(FULL_MASK, (kb >> q) & 1u));
+    for (int j = 0; j < BSEL_G; ++j) cnt += __popc(gt[j] | eq[j]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) cnt += __shfl_xor_sync(FULL_MASK, cnt, o);
     if (lane == 0) sm.wtot[w] = cnt;
     __syncthreads();
     unsigned tot;
     unsigned r = out + bsel_scan_warps<BS>(sm, w, lane, tot);
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      const unsigned bq = __ballot_sync(FULL_MASK, (kb >> q) & 1u);
-      const unsigned rr = r + __popc(bq & lt_mask);
-      if (((kb >> q) & 1u) && rr < static_cast<unsigned>(need_total)) keep[P + rr] = wb + q * 32 + lane;
-      r += __popc(bq);
+    for (int j = 0; j < BSEL_G; ++j) {
+      const uint32_t kb = gt[j] | eq[j];
+      const unsigned c = __popc(kb);
+      unsigned incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o) incl += y;
+      }
+      unsigned rr = r + incl - c;
+      const int i0 = lo + 4 * (pc * BS * BSEL_G + w * 32 * BSEL_G + j * 32 + lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((kb >> e) & 1u) {
+          if (rr < static_cast<unsigned>(need_total)) keep[P + rr] = i0 + e;
+          ++rr;
+        }
+      r += __shfl_sync(FULL_MASK, incl, 31);
     }
     out += tot;
     __syncthreads();

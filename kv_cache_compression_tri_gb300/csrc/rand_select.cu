@@ -22,7 +22,7 @@
 //   3. emission from bitmaps of "above" and "equal" slots in slot order
 //      (per-thread popcounts and one block scan), the equal ones ranked by
 //      slot, so the keep list is ascending without sorting.
-// Shared memory stays small (bitmaps for 65536 slots + the list), so three
+// Shared memory stays small (bitmaps for 65536 slots + the list), so six
 // CTAs share an SM and their phases overlap. Slices with more candidates
 // than the bitmaps cover are emitted in bitmap-sized pieces.
 #include <cuda_runtime.h>
@@ -32,7 +32,7 @@
 namespace tri {
 namespace {
 
-constexpr int RT = 512;             // threads per CTA
+constexpr int RT = 256;             // threads per CTA
 constexpr int RW = RT / 32;         // warps
 constexpr int BM_SLOTS = 65536;     // slots covered by one pair of bitmaps
 constexpr int BM_WORDS = BM_SLOTS / 32;
@@ -163,7 +163,7 @@ __device__ unsigned radix_step(RSmem& sm, const RCtx& c, bool from_list, int nl,
   return cnt;
 }
 
-__global__ void __launch_bounds__(RT, 3) rand_select_kernel(const __grid_constant__ SelectParams p) {
+__global__ void __launch_bounds__(RT, 6) rand_select_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(16) unsigned char rsmem_raw[];
   RSmem& sm = *reinterpret_cast<RSmem*>(rsmem_raw);
   const int t = threadIdx.x, lane = t & 31;

@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
     }
   }
 
-  float* out = p.scores + s * static_cast<int64_t>(p.n_cap);
+  float* out = p.scores + s * p.score_stride;
   uint32_t kmin = 0xffffffffu, kmax = 0u;  // score keys written (fused select)
   bool nan_seen = false;
   const int32_t* pos = EXPLICIT_POS ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;

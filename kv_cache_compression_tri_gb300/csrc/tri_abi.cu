@@ -172,6 +172,7 @@ tri_status prepare_score(const tri_kv* kv, const tri_centers* c, double rope_the
   p.scores = scores;
   p.dev_status = kv->dev_status;
   p.slice_stride = kv->slice_stride;
+  p.score_stride = kv->n_cap;
   p.n_cap = kv->n_cap;
   p.lh_count = kv->n_layers * kv->n_kv_heads;
   p.n_prompt = n_prompt;
@@ -203,8 +204,12 @@ CompactParams compact_params(const tri_kv* kv, const int32_t* keep_idx, int32_t 
   return p;
 }
 
+// The fused path keeps its scores with rows padded to 16 bytes so that the
+// selecting CTA can read them 16 bytes at a time.
+int64_t compress_score_stride(const tri_kv* kv) { return (static_cast<int64_t>(kv->n_cap) + 3) / 4 * 4; }
+
 size_t compress_state_offset(const tri_kv* kv) {
-  const size_t scores = static_cast<size_t>(slices_of(kv)) * kv->n_cap * sizeof(float);
+  const size_t scores = static_cast<size_t>(slices_of(kv)) * compress_score_stride(kv) * sizeof(float);
   return (scores + 255) / 256 * 256;
 }
 
@@ -245,6 +250,7 @@ tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_thet
   st = prepare_score(kv, c, rope_theta, style, norm_mode, offsets, n_offsets, p_cur, n_prompt, n_recent,
                      static_cast<float*>(ws), true, p);
   if (st != TRI_OK) return st;
+  p.score_stride = compress_score_stride(kv);
   p.state = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + compress_state_offset(kv));
   p.keep = keep_idx;
   p.budget = budget;

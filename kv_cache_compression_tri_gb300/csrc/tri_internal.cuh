@@ -187,6 +187,7 @@ struct ScoreParams {
   float* scores;
   int32_t* dev_status;
   int64_t slice_stride;  // elements
+  int64_t score_stride;  // floats between slices of `scores`
   int32_t n_cap;
   int32_t lh_count;  // n_layers * n_kv_heads
   int32_t n_prompt, n_recent;

@@ -254,7 +254,8 @@ def test_qwen3_stack_full_size_compress():
     keep_all = keep.cpu().numpy()
     _structural(keep_all, n, P, W, B)
     assert torch.all(kv.n_valid == B)
-    fs = ws[: S * n_cap * 4].view(torch.float32).view(S, n_cap)
+    stride = (n_cap + 3) // 4 * 4
+    fs = ws[: S * stride * 4].view(torch.float32).view(S, stride)
     gc, gm, gR = f64(c.center), f64(c.mean_norm), f64(c.mrl)
     gs = {s: fs[s].cpu().numpy() for s in sample}
 

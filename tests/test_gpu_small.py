@@ -398,8 +398,10 @@ def _compress_vs_separate(w, ragged=False, explicit_pos=False, seed=0, style=0):
     nk = kv_a.n_valid.cpu().numpy()
     for s in range(S):
         assert torch.equal(kv_a.pos_out[s, :nk[s]], kv_b.pos_out[s, :nk[s]])
-    # the fused scores left in the workspace are the separate call's scores
-    fs = ws[: S * n_cap * 4].view(torch.float32).view(S, n_cap)
+    # the fused scores left in the workspace (rows padded to 4 floats) are
+    # the separate call's scores
+    stride = (n_cap + 3) // 4 * 4
+    fs = ws[: S * stride * 4].view(torch.float32).view(S, stride)
     nv_h = inp.n_valid.cpu().numpy()
     for s in range(S):
         lo, hi = P, int(nv_h[s]) - W
@@ -420,3 +422,6 @@ def test_compress_ragged_explicit_positions_and_styles():
     w2 = synth.scaled(TINY, dtype=torch.bfloat16, n_kv_heads=6, n_cap=3000, n_valid=3000, budget=700,
                       n_prompt=0, n_recent=0)
     _compress_vs_separate(w2, ragged=True, seed=3)
+    w3 = synth.scaled(TINY, dtype=torch.bfloat16, n_kv_heads=5, n_cap=1001, n_valid=1001, budget=333,
+                      n_prompt=3, n_recent=5)  # rows not a multiple of 4
+    _compress_vs_separate(w3, ragged=True, seed=4)
