@@ -283,14 +283,14 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, path: str = "fused") -> dict:
+def workload_config(w, path: str = "separate") -> dict:
     return {
         "workload": w.name, "n_seq": w.n_seq, "n_layers": w.n_layers, "n_kv_heads": w.n_kv_heads,
         "head_dim": w.head_dim, "n_cap": w.n_cap, "n_valid": w.n_valid, "budget": w.budget,
         "n_prompt": w.n_prompt, "n_recent": w.n_recent, "offsets": len(w.offsets),
         "rope_theta": w.theta, "storage": "bf16" if w.elem_bytes == 2 else "f32",
         "path": ("rand_evict + tri_compact_kv" if w.random else
-                 ("tri_compress (fused score+select, then compaction)" if path == "fused" else
+                 ("tri_compress (score, select, compact in one call)" if path == "compress" else
                   "tri_score + tri_select_topk + tri_compact_kv")),
         "parallelism": "one cache batch per GPU (weak scaling)",
     }
@@ -333,7 +333,7 @@ def run_gpu(args, w):
     n_valid = torch.full((S,), n, dtype=torch.int32, device=dev)
     pos_out = torch.empty(S, w.n_cap, dtype=torch.int32, device=dev)
     kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status)
-    fused = (args.path == "fused") and not w.random
+    fused = (args.path == "compress") and not w.random
     scores = None if fused else torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
     keep = torch.empty(S, B, dtype=torch.int32, device=dev)
     cws = torch.empty(tri.compress_workspace_bytes(kv), dtype=torch.uint8, device=dev) if fused else None
@@ -348,7 +348,7 @@ def run_gpu(args, w):
 
     def step(rec=None):
         if fused:
-            # one entry point: score + select in one kernel, then compaction
+            # one entry point (tri_compress): its three kernels in one call
             if rec: rec[0].record(stream)
             tri.compress(kv, centers, w.theta, w.offsets, inp.p_cur, P, W, B, keep, workspace=cws)
             if rec:
@@ -418,13 +418,10 @@ def run_gpu(args, w):
     step_bytes = score_bytes + compact_bytes
     mean = lambda xs: sum(xs) / len(xs)
     peak, peak_kind = measured_peak_gbs()
-    if fused:
-        # the fused call's kernels are timed apart on a separate pass below
-        k1_ms, k2_ms, k3_ms = fused_breakdown(args, tri, kv, centers, w, inp, keep, cws, restore, stream)
     if w.random:
         dom_name, dom_ms, dom_bytes = "compact_kernel", mean(k3_ms), compact_bytes
     else:
-        dom_name, dom_ms, dom_bytes = ("score_select_kernel" if fused else "score_kernel"), mean(k1_ms), score_bytes
+        dom_name, dom_ms, dom_bytes = "score_kernel", mean(k1_ms), score_bytes
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = known_traffic(w.name, dom_name)
     result = {
@@ -437,7 +434,7 @@ def run_gpu(args, w):
         "gbs": step_bytes / (dev_sec / args.steps) / 1e9,
         "hbm_frac_of_8tbs": step_bytes / (dev_sec / args.steps) / 1e9 / 8000.0,
         "algorithmic_bytes_per_step": step_bytes,
-        "kernel_ms": ({"score_select": round(mean(k1_ms), 4), "compact": round(mean(k3_ms), 4)} if fused else
+        "kernel_ms": ({"compress": round(mean(k1_ms), 4)} if fused else
                       {"score" if not w.random else "rand_select": round(mean(k1_ms), 4),
                        "select": round(mean(k2_ms), 4), "compact": round(mean(k3_ms), 4)}),
         "moved_rows_per_step": moved,
@@ -454,46 +451,136 @@ def run_gpu(args, w):
         result["e2e"] = run_e2e(args, w, tri, synth, inp, centers, dev, stream)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, w)
+    if ws == 1 and not args.no_extra and w.name == "qwen3_8b_stack":
+        del inp, centers, k_head, v_head, kv, keep, pos_out
+        torch.cuda.empty_cache()
+        result["other_workloads"] = measure_other(args, tri, synth, dev)
     if rank == 0:
         print(json.dumps(result), flush=True)
     return 0
 
 
-KERNEL_SOURCES = {"score_kernel": "score.cu", "score_select_kernel": "score.cu", "select_kernel": "select.cu",
-                  "compact_kernel": "compact.cu", "rand_select_kernel": "rand_select.cu"}
-
-
-def fused_breakdown(args, tri, kv, centers, w, inp, keep, ws, restore, stream):
-    """Per-kernel times of the fused call: the same three launches issued by
-    hand (state init + score/select kernel, then compaction) with events
-    between them, on restored inputs, outside the timed region."""
-    import ctypes
-
+def measure_other(args, tri, synth, dev):
+    """The other two 32K-token workloads, timed like the main one (CUDA
+    events around each event, first B rows restored between events):
+    Random Attention on the stack, and the large-batch periodic workload
+    (its 32768-row event, then 16 rounds of +128 rows -> 2048 with explicit
+    positions, the appended rows drawn outside the timed region)."""
+    import numpy as np
     import torch
 
-    lib = tri.load_library()
-    P, W, B = w.n_prompt, w.n_recent, w.budget
-    reps = max(3, min(args.steps, 10))
-    k1, k3 = [], []
-    for _ in range(reps):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record(stream)
-        tri.compress(kv, centers, w.theta, w.offsets, inp.p_cur, P, W, B, keep, workspace=ws)
-        e[2].record(stream)
-        torch.cuda.synchronize()
-        restore()
-        # compaction alone on the same keep lists (restored inputs)
-        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        e1[0].record(stream)
+    out = {}
+    peak, _ = measured_peak_gbs()
+    steps = max(3, min(args.steps, 10))
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, restore):
+        ts = []
+        for i in range(args.warmup + steps):
+            restore()
+            a, b = ev(), ev()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ts.append(a.elapsed_time(b))
+        return sum(ts) / len(ts)
+
+    # ---- Random Attention on the stack --------------------------------------
+    w = synth.WORKLOADS["random_stack"]
+    S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    inp = synth.make_inputs(w, dev, with_queries=False)
+    kh, vh = inp.k[:, :, :, :B].clone(), inp.v[:, :, :, :B].clone()
+    nv = torch.full((S,), n, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = tri.KVCache(inp.k, inp.v, nv, None, torch.empty(S, w.n_cap, dtype=torch.int32, device=dev), st)
+    keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+
+    def restore_r():
+        inp.k[:, :, :, :B].copy_(kh)
+        inp.v[:, :, :, :B].copy_(vh)
+        nv.fill_(n)
+
+    ms = timed(lambda: (tri.rand_evict(kv, 0, 0, P, W, B, keep), tri.compact_kv(kv, keep, B)), restore_r)
+    moved = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
+    by = moved * (4 * w.head_dim * w.elem_bytes + 8)
+    assert int(st.item()) == 0
+    out[w.name] = {"value": S * n / (ms / 1e3), "unit": UNIT, "ms_per_event": ms, "gbs": by / ms / 1e6,
+                   "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
+                   "algorithmic_bytes": by}
+    del inp, kh, vh, kv, keep
+    torch.cuda.empty_cache()
+
+    # ---- large-batch periodic -----------------------------------------------
+    w = synth.WORKLOADS["periodic_large_batch"]
+    S, n, P, W, B, R, d, e = (w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget, w.round_rows,
+                              w.head_dim, w.elem_bytes)
+    inp = synth.make_inputs(w, dev)
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    torch.cuda.empty_cache()
+    kh, vh = inp.k[:, :, :, :B].clone(), inp.v[:, :, :, :B].clone()
+    nv = torch.full((S,), n, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pos = torch.empty(S, w.n_cap, dtype=torch.int32, device=dev)
+    kv = tri.KVCache(inp.k, inp.v, nv, None, pos, st)
+    scores = torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+    p_cur = inp.p_cur.clone()
+
+    def event():
+        tri.score(kv, c, w.theta, w.offsets, p_cur, scores, n_prompt=P, n_recent=W)
+        tri.select_topk(scores, kv, P, W, B, keep)
         tri.compact_kv(kv, keep, B)
-        e1[1].record(stream)
+
+    def restore_p():
+        inp.k[:, :, :, :B].copy_(kh)
+        inp.v[:, :, :, :B].copy_(vh)
+        nv.fill_(n)
+        kv.pos = None
+
+    ms = timed(event, restore_p)
+    moved = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
+    by = S * (n - P - W) * d * e + moved * (4 * d * e + 8)
+    assert int(st.item()) == 0
+    res = {"pass_32k": {"value": S * n / (ms / 1e3), "unit": UNIT, "ms_per_event": ms, "gbs": by / ms / 1e6,
+                        "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
+                        "algorithmic_bytes": by}}
+    # rounds continue from the state the last timed pass left
+    kv.pos = pos
+    rms, rby = [], []
+    for rnd in range(1, w.rounds + 1):
+        kn, vn = synth.append_rows(inp, rnd, R)
+        inp.k[:, :, :, B:B + R] = kn
+        inp.v[:, :, :, B:B + R] = vn
+        first = n + R * (rnd - 1)
+        pos[:, B:B + R] = torch.arange(first, first + R, dtype=torch.int32, device=dev)[None, :]
+        nv.fill_(B + R)
+        p_cur.fill_(first + R - 1)
+        del kn, vn
+        a, b = ev(), ev()
         torch.cuda.synchronize()
-        restore()
-        tot = e[0].elapsed_time(e[2])
-        c = e1[0].elapsed_time(e1[1])
-        k3.append(c)
-        k1.append(tot - c)
-    return k1, [0.0] * reps, k3
+        a.record()
+        event()
+        b.record()
+        torch.cuda.synchronize()
+        rms.append(a.elapsed_time(b))
+        mv = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
+        rby.append(S * (B + R - P - W) * (d * e + 4) + mv * (4 * d * e + 8))
+    assert int(st.item()) == 0
+    mr = sum(rms) / len(rms)
+    mb = sum(rby) / len(rby)
+    res["rounds"] = {"count": w.rounds, "value": S * (B + R) / (mr / 1e3), "unit": UNIT, "ms_per_round": mr,
+                     "gbs": mb / mr / 1e6, "hbm_frac_of_8tbs": mb / mr / 1e6 / 8000.0}
+    out[w.name] = res
+    del inp, kh, vh, kv, keep, scores, pos
+    torch.cuda.empty_cache()
+    return out
+
+
+KERNEL_SOURCES = {"score_kernel": "score.cu", "select_kernel": "select.cu", "compact_kernel": "compact.cu",
+                  "rand_select_kernel": "rand_select.cu"}
 
 
 def known_traffic(workload: str, kernel: str):
@@ -538,11 +625,11 @@ def run_e2e(args, w, tri, synth, inp, centers, dev, stream):
     pos_out = torch.empty(Se, w.n_cap, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kv = tri.KVCache(dk, dv, n_valid, None, pos_out, status)
-    scores = None if (args.path == "fused" or w.random) else torch.empty(Se, w.n_cap, dtype=torch.float32, device=dev)
+    scores = None
     keep = torch.empty(Se, B, dtype=torch.int32, device=dev)
     p_cur = inp.p_cur[:n_seq]
 
-    fused = (args.path == "fused") and not w.random
+    fused = not w.random  # the end-to-end leg goes through the single public call
     cws = torch.empty(tri.compress_workspace_bytes(kv), dtype=torch.uint8, device=dev) if fused else None
 
     def one():
@@ -604,10 +691,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gpu", "reference", "ours"], default="gpu")
     ap.add_argument("--workload", default="qwen3_8b_stack")
-    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
-                    help="fused: tri_compress; separate: tri_score + tri_select_topk + tri_compact_kv")
+    ap.add_argument("--path", choices=["separate", "compress"], default="separate",
+                    help="separate: tri_score + tri_select_topk + tri_compact_kv (per-kernel events); "
+                         "compress: the single tri_compress call")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other 32K-token workloads")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-max-seqs", type=int, default=16)
     ap.add_argument("--cpu-slices", type=int, default=32)

@@ -236,15 +236,13 @@ tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n
 
 /* ------------------------------------------------------------------------
  * tri_compress -- one compression event: score + select + compact.
- * The same result as tri_score (rows [n_prompt, n_valid - n_recent)),
- * tri_select_topk and tri_compact_kv called in sequence with the same
- * arguments, in two launches: the scoring kernel also selects (the last CTA
- * to finish scoring a slice selects that slice from its fresh scores while
- * other CTAs keep streaming keys), then the compaction kernel runs.
+ * Exactly tri_score (rows [n_prompt, n_valid - n_recent)), tri_select_topk
+ * and tri_compact_kv called in sequence with the same arguments (three
+ * launches on the stream), with the scores kept in caller scratch.
  * keep_idx: device [n_slices][budget], written as by tri_select_topk.
  * ws: device scratch of at least tri_compress_workspace_bytes(kv) bytes,
- * 16-byte aligned (scores and per-slice selection state; nothing in it needs
- * to be initialised or survives the call). kv->pos_out required.
+ * 16-byte aligned (the scores [n_slices][n_cap]; nothing in it needs to be
+ * initialised or survives the call). kv->pos_out required.
  * ------------------------------------------------------------------------ */
 size_t tri_compress_workspace_bytes(const tri_kv* kv);
 tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_theta,

@@ -28,15 +28,9 @@
 //     butterfly that leaves consecutive scores in consecutive lanes.
 // Every wait on a tile is bounded in wall-clock time; a timeout records
 // TRI_DEV_TIMEOUT, drains the copies in flight and leaves the tile unscored.
-//
-// Fused variant (tri_compress): each CTA also folds the keys of the scores it
-// wrote into a per-slice min / max and takes a ticket; the CTA holding the
-// slice's last ticket then selects that slice (block_select.cuh) from its
-// freshly written scores, reusing its tile ring as scratch, while the other
-// CTAs keep streaming keys.
+
 #include <cuda_runtime.h>
 
-#include "block_select.cuh"
 #include "tri_internal.cuh"
 
 namespace tri {
@@ -124,7 +118,7 @@ __device__ __forceinline__ float reduce_scatter(float (&a)[NU], int lane, int& i
   return r;
 }
 
-template <typename T, int D, int STYLE, bool EXPLICIT_POS, bool FUSED>
+template <typename T, int D, int STYLE, bool EXPLICIT_POS>
 __global__ void __launch_bounds__(SCORE_THREADS, 3)
     score_kernel(const __grid_constant__ ScoreParams p) {
   using G = Geo<T, D>;
@@ -146,8 +140,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   }
   const int c0 = max(ct * p.rows_per_cta, p.n_prompt);
   const int c1 = min((ct + 1) * p.rows_per_cta, n - p.n_recent);
-  if (!FUSED && c0 >= c1) return;  // uniform over the CTA
-  const int ntiles = (c0 < c1) ? (c1 - c0 + TILE_ROWS - 1) / TILE_ROWS : 0;
+  if (c0 >= c1) return;  // uniform over the CTA
+  const int ntiles = (c1 - c0 + TILE_ROWS - 1) / TILE_ROWS;
   const unsigned char* src =
       static_cast<const unsigned char*>(p.k) + (s * p.slice_stride + static_cast<int64_t>(c0) * D) * sizeof(T);
 
@@ -214,9 +208,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
     }
   }
 
-  float* out = p.scores + s * p.score_stride;
-  uint32_t kmin = 0xffffffffu, kmax = 0u;  // score keys written (fused select)
-  bool nan_seen = false;
+  float* out = p.scores + s * static_cast<int64_t>(p.n_cap);
   const int32_t* pos = EXPLICIT_POS ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
 
   int t = 0;
@@ -284,14 +276,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
       int idx;
       const float v = reduce_scatter<TPK, STEPS>(acc, lane, idx);
       const int r = c0 + t * TILE_ROWS + rbase + idx * KPW;
-      if ((c % (TPK / STEPS)) == 0 && r < c1) {
-        __stcs(out + r, v);
-        if (FUSED) {
-          const uint32_t k = score_key(v, nan_seen);
-          kmin = min(kmin, k);
-          kmax = max(kmax, k);
-        }
-      }
+      if ((c % (TPK / STEPS)) == 0 && r < c1) __stcs(out + r, v);
     }
     __syncthreads();  // the whole CTA is done with stage st
     if (*failed) break;
@@ -307,36 +292,11 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
     for (int u = t; u < min(ntiles, t + STAGES); ++u)
       (void)mbar_wait_bounded(&full[u % STAGES], static_cast<uint32_t>((u / STAGES) & 1));
   }
-  if (FUSED) {
-    // Publish this CTA's key range, then take a ticket; the CTA that takes
-    // the slice's last ticket selects the slice (every score of it is
-    // written and made visible by the fences before the tickets).
-    uint32_t* st = p.state + 3 * s;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      kmin = min(kmin, __shfl_xor_sync(FULL_MASK, kmin, o));
-      kmax = max(kmax, __shfl_xor_sync(FULL_MASK, kmax, o));
-    }
-    if (lane == 0 && kmin <= kmax) {
-      atomicMin(st + 1, kmin);
-      atomicMax(st + 2, kmax);
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *failed = (atomicAdd(st, 1u) == static_cast<uint32_t>(p.tiles_per_slice - 1)) ? 2 : 0;
-    __syncthreads();
-    if (*failed == 2) {
-      __threadfence();
-      const uint32_t smin = __ldcg(st + 1), smax = __ldcg(st + 2);
-      block_select<SCORE_THREADS>(out, n, p.n_prompt, p.n_recent, p.budget, smin, smax,
-                                  p.keep + s * static_cast<int64_t>(p.budget), ring, p.dev_status);
-    }
-  }
 }
 
-template <typename T, int D, int STYLE, bool EXPLICIT_POS, bool FUSED>
+template <typename T, int D, int STYLE, bool EXPLICIT_POS>
 cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
-  auto kern = score_kernel<T, D, STYLE, EXPLICIT_POS, FUSED>;
+  auto kern = score_kernel<T, D, STYLE, EXPLICIT_POS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SCORE_SMEM));
   if (e != cudaSuccess) return e;
@@ -346,31 +306,14 @@ cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <typename T, int D, bool FUSED>
+template <typename T, int D>
 cudaError_t launch_style(const ScoreParams& p, tri_rope_style style, bool explicit_pos, int n_slices,
                          cudaStream_t st) {
   if (style == TRI_ROPE_INTERLEAVED)
-    return explicit_pos ? launch_one<T, D, TRI_ROPE_INTERLEAVED, true, FUSED>(p, n_slices, st)
-                        : launch_one<T, D, TRI_ROPE_INTERLEAVED, false, FUSED>(p, n_slices, st);
-  return explicit_pos ? launch_one<T, D, TRI_ROPE_HALF, true, FUSED>(p, n_slices, st)
-                      : launch_one<T, D, TRI_ROPE_HALF, false, FUSED>(p, n_slices, st);
-}
-
-template <typename T, int D>
-cudaError_t launch_dim(const ScoreParams& p, tri_rope_style style, bool explicit_pos, int n_slices,
-                       cudaStream_t st, bool fused) {
-  return fused ? launch_style<T, D, true>(p, style, explicit_pos, n_slices, st)
-               : launch_style<T, D, false>(p, style, explicit_pos, n_slices, st);
-}
-
-// Per-slice state of the fused path: no tickets, empty key range.
-__global__ void fused_state_init(uint32_t* state, int64_t n_slices) {
-  const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-  if (i < n_slices) {
-    state[3 * i] = 0u;
-    state[3 * i + 1] = 0xffffffffu;
-    state[3 * i + 2] = 0u;
-  }
+    return explicit_pos ? launch_one<T, D, TRI_ROPE_INTERLEAVED, true>(p, n_slices, st)
+                        : launch_one<T, D, TRI_ROPE_INTERLEAVED, false>(p, n_slices, st);
+  return explicit_pos ? launch_one<T, D, TRI_ROPE_HALF, true>(p, n_slices, st)
+                      : launch_one<T, D, TRI_ROPE_HALF, false>(p, n_slices, st);
 }
 
 template <typename T, int D>
@@ -387,19 +330,13 @@ ScoreGeometry score_geometry(tri_dtype dt, int head_dim) {
 }
 
 cudaError_t launch_score(const ScoreParams& p, tri_dtype dt, int head_dim, tri_rope_style style,
-                         bool explicit_pos, int n_slices, cudaStream_t st, bool fused) {
-  if (fused) {
-    fused_state_init<<<static_cast<unsigned>((n_slices + 255) / 256), 256, 0, st>>>(p.state, n_slices);
-    note_launch();
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+                         bool explicit_pos, int n_slices, cudaStream_t st) {
   if (dt == TRI_BF16) {
-    if (head_dim == 128) return launch_dim<uint16_t, 128>(p, style, explicit_pos, n_slices, st, fused);
-    return launch_dim<uint16_t, 64>(p, style, explicit_pos, n_slices, st, fused);
+    if (head_dim == 128) return launch_style<uint16_t, 128>(p, style, explicit_pos, n_slices, st);
+    return launch_style<uint16_t, 64>(p, style, explicit_pos, n_slices, st);
   }
-  if (head_dim == 128) return launch_dim<float, 128>(p, style, explicit_pos, n_slices, st, fused);
-  return launch_dim<float, 64>(p, style, explicit_pos, n_slices, st, fused);
+  if (head_dim == 128) return launch_style<float, 128>(p, style, explicit_pos, n_slices, st);
+  return launch_style<float, 64>(p, style, explicit_pos, n_slices, st);
 }
 
 }  // namespace tri

@@ -172,7 +172,6 @@ tri_status prepare_score(const tri_kv* kv, const tri_centers* c, double rope_the
   p.scores = scores;
   p.dev_status = kv->dev_status;
   p.slice_stride = kv->slice_stride;
-  p.score_stride = kv->n_cap;
   p.n_cap = kv->n_cap;
   p.lh_count = kv->n_layers * kv->n_kv_heads;
   p.n_prompt = n_prompt;
@@ -204,13 +203,20 @@ CompactParams compact_params(const tri_kv* kv, const int32_t* keep_idx, int32_t 
   return p;
 }
 
-// The fused path keeps its scores with rows padded to 16 bytes so that the
-// selecting CTA can read them 16 bytes at a time.
-int64_t compress_score_stride(const tri_kv* kv) { return (static_cast<int64_t>(kv->n_cap) + 3) / 4 * 4; }
-
-size_t compress_state_offset(const tri_kv* kv) {
-  const size_t scores = static_cast<size_t>(slices_of(kv)) * compress_score_stride(kv) * sizeof(float);
-  return (scores + 255) / 256 * 256;
+SelectParams select_params(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
+                           int32_t budget, int32_t* keep_idx) {
+  SelectParams p{};
+  p.scores = scores;
+  p.n_valid = kv->n_valid;
+  p.keep = keep_idx;
+  p.dev_status = kv->dev_status;
+  p.n_cap = kv->n_cap;
+  p.n_prompt = n_prompt;
+  p.n_recent = n_recent;
+  p.budget = budget;
+  p.n_layers = kv->n_layers;
+  p.n_kv_heads = kv->n_kv_heads;
+  return p;
 }
 
 }  // namespace
@@ -233,7 +239,7 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
 
 size_t tri_compress_workspace_bytes(const tri_kv* kv) {
   if (check_kv(kv, false) != TRI_OK) return 0;
-  return compress_state_offset(kv) + static_cast<size_t>(slices_of(kv)) * 3 * sizeof(uint32_t);
+  return static_cast<size_t>(slices_of(kv)) * kv->n_cap * sizeof(float);
 }
 
 tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_theta, tri_rope_style style,
@@ -247,17 +253,16 @@ tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_thet
   tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
   if (st != TRI_OK) return st;
   ScoreParams p;
+  float* scores = static_cast<float*>(ws);
   st = prepare_score(kv, c, rope_theta, style, norm_mode, offsets, n_offsets, p_cur, n_prompt, n_recent,
-                     static_cast<float*>(ws), true, p);
+                     scores, true, p);
   if (st != TRI_OK) return st;
-  p.score_stride = compress_score_stride(kv);
-  p.state = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + compress_state_offset(kv));
-  p.keep = keep_idx;
-  p.budget = budget;
-  cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, kv->pos != nullptr,
-                               static_cast<int>(slices_of(kv)), stream, true);
+  const int n_slices = static_cast<int>(slices_of(kv));
+  cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, kv->pos != nullptr, n_slices, stream);
   if (e != cudaSuccess) return TRI_ERR_CUDA;
-  e = launch_compact(compact_params(kv, keep_idx, budget), static_cast<int>(slices_of(kv)), stream);
+  e = launch_select(select_params(scores, kv, n_prompt, n_recent, budget, keep_idx), n_slices, stream);
+  if (e != cudaSuccess) return TRI_ERR_CUDA;
+  e = launch_compact(compact_params(kv, keep_idx, budget), n_slices, stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 
@@ -271,18 +276,8 @@ tri_status tri_select_topk(const float* scores, const tri_kv* kv, int32_t n_prom
   tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
   if (st != TRI_OK) return st;
   if (slices_of(kv) > 0x7fffffff) return TRI_ERR_INVALID_ARG;
-  SelectParams p{};
-  p.scores = scores;
-  p.n_valid = kv->n_valid;
-  p.keep = keep_idx;
-  p.dev_status = kv->dev_status;
-  p.n_cap = kv->n_cap;
-  p.n_prompt = n_prompt;
-  p.n_recent = n_recent;
-  p.budget = budget;
-  p.n_layers = kv->n_layers;
-  p.n_kv_heads = kv->n_kv_heads;
-  const cudaError_t e = launch_select(p, static_cast<int>(slices_of(kv)), stream);
+  const cudaError_t e = launch_select(select_params(scores, kv, n_prompt, n_recent, budget, keep_idx),
+                                      static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 
@@ -295,16 +290,7 @@ tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n
   tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
   if (st != TRI_OK) return st;
   if (slices_of(kv) > 0x7fffffff) return TRI_ERR_INVALID_ARG;
-  SelectParams p{};
-  p.n_valid = kv->n_valid;
-  p.keep = keep_idx;
-  p.dev_status = kv->dev_status;
-  p.n_cap = kv->n_cap;
-  p.n_prompt = n_prompt;
-  p.n_recent = n_recent;
-  p.budget = budget;
-  p.n_layers = kv->n_layers;
-  p.n_kv_heads = kv->n_kv_heads;
+  SelectParams p = select_params(nullptr, kv, n_prompt, n_recent, budget, keep_idx);
   p.seed = seed;
   p.round = round;
   const cudaError_t e = launch_rand_select(p, static_cast<int>(slices_of(kv)), stream);

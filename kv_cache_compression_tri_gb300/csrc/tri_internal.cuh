@@ -187,7 +187,6 @@ struct ScoreParams {
   float* scores;
   int32_t* dev_status;
   int64_t slice_stride;  // elements
-  int64_t score_stride;  // floats between slices of `scores`
   int32_t n_cap;
   int32_t lh_count;  // n_layers * n_kv_heads
   int32_t n_prompt, n_recent;
@@ -201,11 +200,6 @@ struct ScoreParams {
   float step_im[MAX_BANDS];
   float jump_re[MAX_BANDS];   // e^{-i omega_f * (positions skipped between tiles)}
   float jump_im[MAX_BANDS];
-  // fused score + select only: per-slice state {tickets, min key, max key}
-  // and the keep lists the last CTA of each slice writes
-  uint32_t* state;
-  int32_t* keep;
-  int32_t budget;
 };
 
 struct SelectParams {
@@ -246,7 +240,7 @@ struct CalibParams {
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_score(const ScoreParams& p, tri_dtype dt, int head_dim, tri_rope_style style,
-                         bool explicit_pos, int n_slices, cudaStream_t st, bool fused = false);
+                         bool explicit_pos, int n_slices, cudaStream_t st);
 // Score kernel geometry, shared by the launcher and the host constant table:
 // positions between consecutive keys of one lane inside a tile, and the
 // positions skipped from a lane's last key of a tile to its first of the next.

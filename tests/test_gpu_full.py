@@ -231,7 +231,7 @@ def test_periodic_large_batch_full_size():
 
 
 def test_qwen3_stack_full_size_compress():
-    """The fused entry point at full size: keep lists follow the oracle on
+    """The single-call entry point at full size: keep lists follow the oracle on
     sampled slices (exactly, on the fp32 scores it left in its workspace, and
     by the near-tie rule against fp64 scores) and the structural invariants
     hold for every slice."""
@@ -254,8 +254,7 @@ def test_qwen3_stack_full_size_compress():
     keep_all = keep.cpu().numpy()
     _structural(keep_all, n, P, W, B)
     assert torch.all(kv.n_valid == B)
-    stride = (n_cap + 3) // 4 * 4
-    fs = ws[: S * stride * 4].view(torch.float32).view(S, stride)
+    fs = ws[: S * n_cap * 4].view(torch.float32).view(S, n_cap)
     gc, gm, gR = f64(c.center), f64(c.mean_norm), f64(c.mrl)
     gs = {s: fs[s].cpu().numpy() for s in sample}
 

@@ -390,7 +390,7 @@ def _compress_vs_separate(w, ragged=False, explicit_pos=False, seed=0, style=0):
     n0 = tri.launch_count()
     tri.compress(kv_b, c, w.theta, w.offsets, inp.p_cur, P, W, B, keep_b, workspace=ws, style=style)
     torch.cuda.synchronize()
-    assert tri.launch_count() - n0 == 3  # state init, score+select, compaction
+    assert tri.launch_count() - n0 == 3  # score, select, compaction
     assert int(kv_a.dev_status.item()) == 0 and int(kv_b.dev_status.item()) == 0
     assert torch.equal(keep_a, keep_b)
     assert torch.equal(kv_a.k, kv_b.k) and torch.equal(kv_a.v, kv_b.v)
@@ -398,10 +398,8 @@ def _compress_vs_separate(w, ragged=False, explicit_pos=False, seed=0, style=0):
     nk = kv_a.n_valid.cpu().numpy()
     for s in range(S):
         assert torch.equal(kv_a.pos_out[s, :nk[s]], kv_b.pos_out[s, :nk[s]])
-    # the fused scores left in the workspace (rows padded to 4 floats) are
-    # the separate call's scores
-    stride = (n_cap + 3) // 4 * 4
-    fs = ws[: S * stride * 4].view(torch.float32).view(S, stride)
+    # the scores left in the workspace are the separate call's scores
+    fs = ws[: S * n_cap * 4].view(torch.float32).view(S, n_cap)
     nv_h = inp.n_valid.cpu().numpy()
     for s in range(S):
         lo, hi = P, int(nv_h[s]) - W
