@@ -547,22 +547,31 @@ def measure_other(args, tri, synth, dev):
     res = {"pass_32k": {"value": S * n / (ms / 1e3), "unit": UNIT, "ms_per_event": ms, "gbs": by / ms / 1e6,
                         "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
                         "algorithmic_bytes": by}}
-    # rounds continue from the state the last timed pass left
-    kv.pos = pos
+    # rounds continue from the state the last timed pass left; in steady state
+    # only B + R rows of each slice are in use, so the rounds see a cache view
+    # of capacity B + R (same storage and slice stride, positions and scores
+    # laid out [S][B + R])
+    cap = B + R
+    pos2 = pos[:, :cap].clone()
+    nv2 = torch.full((S,), B, dtype=torch.int32, device=dev)
+    kv2 = tri.KVCache(inp.k[:, :, :, :cap], inp.v[:, :, :, :cap], nv2, pos2, pos2, st)
+    scores2 = torch.empty(S, cap, dtype=torch.float32, device=dev)
     rms, rby = [], []
     for rnd in range(1, w.rounds + 1):
         kn, vn = synth.append_rows(inp, rnd, R)
         inp.k[:, :, :, B:B + R] = kn
         inp.v[:, :, :, B:B + R] = vn
         first = n + R * (rnd - 1)
-        pos[:, B:B + R] = torch.arange(first, first + R, dtype=torch.int32, device=dev)[None, :]
-        nv.fill_(B + R)
+        pos2[:, B:B + R] = torch.arange(first, first + R, dtype=torch.int32, device=dev)[None, :]
+        nv2.fill_(B + R)
         p_cur.fill_(first + R - 1)
         del kn, vn
         a, b = ev(), ev()
         torch.cuda.synchronize()
         a.record()
-        event()
+        tri.score(kv2, c, w.theta, w.offsets, p_cur, scores2, n_prompt=P, n_recent=W)
+        tri.select_topk(scores2, kv2, P, W, B, keep)
+        tri.compact_kv(kv2, keep, B)
         b.record()
         torch.cuda.synchronize()
         rms.append(a.elapsed_time(b))
@@ -572,9 +581,10 @@ def measure_other(args, tri, synth, dev):
     mr = sum(rms) / len(rms)
     mb = sum(rby) / len(rby)
     res["rounds"] = {"count": w.rounds, "value": S * (B + R) / (mr / 1e3), "unit": UNIT, "ms_per_round": mr,
-                     "gbs": mb / mr / 1e6, "hbm_frac_of_8tbs": mb / mr / 1e6 / 8000.0}
+                     "gbs": mb / mr / 1e6, "hbm_frac_of_8tbs": mb / mr / 1e6 / 8000.0,
+                     "view": "capacity B + 128 rows per slice (steady state)"}
     out[w.name] = res
-    del inp, kh, vh, kv, keep, scores, pos
+    del inp, kh, vh, kv, kv2, keep, scores, scores2, pos, pos2
     torch.cuda.empty_cache()
     return out
 

@@ -32,15 +32,25 @@
 namespace tri {
 namespace {
 
-constexpr int NT = 1024;
-constexpr int NW = NT / 32;
-constexpr int KCAP = 32768;       // keys staged per super-chunk
-constexpr int WSPAN = KCAP / NW;  // slots per warp (1024)
-constexpr int NQ = WSPAN / 32;    // steps per lane (32)
-constexpr int LCAP = 4096;        // short-list capacity
-constexpr size_t SEL_SMEM = KCAP * sizeof(uint32_t)              // keys
-                            + NW * 256 * sizeof(unsigned)         // per-warp histograms
-                            + LCAP * sizeof(uint32_t);            // short list
+// Launch geometry: NT threads, up to KCAP keys staged per super-chunk; warp w
+// owns slots [WSPAN w, WSPAN (w+1)) of a super-chunk and lane l reads slot
+// WSPAN w + 32 q + l at step q.
+template <int NT_, int KCAP_, int LCAP_, int MINB_>
+struct SelGeo {
+  static constexpr int NT = NT_;
+  static constexpr int MINB = MINB_;  // CTAs per SM the registers must allow
+  static constexpr int NW = NT / 32;
+  static constexpr int KCAP = KCAP_;
+  static constexpr int WSPAN = KCAP / NW;
+  static constexpr int NQ = WSPAN / 32;
+  static constexpr int LCAP = LCAP_;  // short-list capacity
+  static constexpr size_t SMEM = KCAP * sizeof(uint32_t)          // keys
+                                 + NW * 256 * sizeof(unsigned)     // per-warp histograms
+                                 + LCAP * sizeof(uint32_t);        // short list
+  static_assert(NQ == 32 && WSPAN % 128 == 0, "select geometry");
+};
+using BigGeo = SelGeo<1024, 32768, 4096, 1>;  // 32K-row slices: one CTA per SM
+using SmallGeo = SelGeo<256, 8192, 1024, 4>;  // short slices: four CTAs per SM
 
 struct SliceCtx {
   int64_t s;
@@ -50,6 +60,7 @@ struct SliceCtx {
   int seq, layer, head;
 };
 
+template <int NW>
 struct Smem {
   unsigned hist[256];
   unsigned wtot[NW];
@@ -67,8 +78,10 @@ __device__ __forceinline__ bool in_range(int i, int lo, int hi) {
 // Stage the keys of slots [base, base + KCAP) into skey (slot-ordered).
 // Slots outside [P, end) get key 0 and are masked out by their index later.
 // Accumulates this thread's min / max over the valid keys it staged.
+template <class G>
 __device__ __forceinline__ void stage_keys(const SelectParams& p, const SliceCtx& c, int base,
                                            uint32_t* skey, bool& nan, uint32_t& kmin, uint32_t& kmax) {
+  constexpr int WSPAN = G::WSPAN;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int V = WSPAN / 4 / 32;  // 16-byte groups per lane (8)
   const float* row = p.scores + c.s * static_cast<int64_t>(p.n_cap);
@@ -109,7 +122,8 @@ __device__ __forceinline__ void stage_keys(const SelectParams& p, const SliceCtx
 
 // Warp 0 finds digit b with count(digits > b) < need <= count(digits >= b)
 // and publishes (b, count above b, count of b). Caller syncs around it.
-__device__ __forceinline__ void pick_bin(Smem& sm, unsigned need, int lane) {
+template <class SM>
+__device__ __forceinline__ void pick_bin(SM& sm, unsigned need, int lane) {
   unsigned h[8], ls = 0u;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -140,8 +154,9 @@ __device__ __forceinline__ void pick_bin(Smem& sm, unsigned need, int lane) {
 
 // Exclusive prefix of this warp's entry among the 32 warp totals in
 // sm.wtot, and the grand total (every warp computes it redundantly).
-__device__ __forceinline__ unsigned warp_offset(const Smem& sm, int w, int lane, unsigned& total) {
-  const unsigned x = sm.wtot[lane];
+template <int NW>
+__device__ __forceinline__ unsigned warp_offset(const Smem<NW>& sm, int w, int lane, unsigned& total) {
+  const unsigned x = (lane < NW) ? sm.wtot[lane] : 0u;
   unsigned incl = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -152,11 +167,13 @@ __device__ __forceinline__ unsigned warp_offset(const Smem& sm, int w, int lane,
   return __shfl_sync(FULL_MASK, incl - x, w);
 }
 
-__global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ SelectParams p) {
+template <class G>
+__global__ void __launch_bounds__(G::NT, G::MINB) select_kernel(const __grid_constant__ SelectParams p) {
+  constexpr int NT = G::NT, NW = G::NW, KCAP = G::KCAP, WSPAN = G::WSPAN, NQ = G::NQ, LCAP = G::LCAP;
   extern __shared__ __align__(16) uint32_t skey[];
   unsigned* whist = skey + KCAP;  // [NW][256]
   uint32_t* lkey = whist + NW * 256;
-  __shared__ Smem sm;
+  __shared__ Smem<NW> sm;
 
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   SliceCtx c;
@@ -202,7 +219,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
 
   if (staged_once) {
     uint32_t kmin = 0xffffffffu, kmax = 0u;
-    stage_keys(p, c, c.lo, skey, nan, kmin, kmax);
+    stage_keys<G>(p, c, c.lo, skey, nan, kmin, kmax);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       kmin = min(kmin, __shfl_xor_sync(FULL_MASK, kmin, o));
@@ -213,8 +230,8 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
       sm.wmax[w] = kmax;
     }
     __syncthreads();
-    kmin = sm.wmin[lane];
-    kmax = sm.wmax[lane];
+    kmin = (lane < NW) ? sm.wmin[lane] : 0xffffffffu;
+    kmax = (lane < NW) ? sm.wmax[lane] : 0u;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       kmin = min(kmin, __shfl_xor_sync(FULL_MASK, kmin, o));
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
       if (!staged_once) {
         uint32_t a = 0xffffffffu, b = 0u;
         __syncthreads();  // previous users of skey are done
-        stage_keys(p, c, base, skey, nan, a, b);
+        stage_keys<G>(p, c, base, skey, nan, a, b);
         __syncthreads();
       }
 #pragma unroll 8
@@ -256,11 +273,11 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
       }
     }
     __syncthreads();
-    if (t < 256) {
+    for (int b = t; b < 256; b += NT) {
       unsigned sum = 0u;
 #pragma unroll 8
-      for (int ww = 0; ww < NW; ++ww) sum += whist[ww * 256 + t];
-      sm.hist[t] = sum;
+      for (int ww = 0; ww < NW; ++ww) sum += whist[ww * 256 + b];
+      sm.hist[b] = sum;
     }
     __syncthreads();
     if (w == 0) pick_bin(sm, need, lane);
@@ -304,7 +321,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
     __syncthreads();
     const int nl = static_cast<int>(sm.nlist);
     while (!resolved) {
-      if (t < 256) sm.hist[t] = 0u;
+      for (int b = t; b < 256; b += NT) sm.hist[b] = 0u;
       __syncthreads();
       const uint32_t dmask = (1u << width) - 1u;
       for (int e = t; e < nl; e += NT) {
@@ -342,7 +359,7 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
     if (!staged_once) {
       uint32_t a = 0xffffffffu, b = 0u;
       __syncthreads();
-      stage_keys(p, c, base, skey, nan, a, b);
+      stage_keys<G>(p, c, base, skey, nan, a, b);
       __syncthreads();
     }
     uint32_t eqb = 0u, gtb = 0u;
@@ -394,17 +411,26 @@ __global__ void __launch_bounds__(NT, 1) select_kernel(const __grid_constant__ S
   if (t == 0 && sm.nan_seen) set_status(p.dev_status, TRI_DEV_NAN_SCORE);
 }
 
+template <class G>
+cudaError_t launch_geo(const SelectParams& p, int n_slices, cudaStream_t st) {
+  // The dynamic shared memory opt-in is a per-device function attribute;
+  // setting it on every call is cheap and covers every device.
+  const cudaError_t e = cudaFuncSetAttribute(select_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(G::SMEM));
+  if (e != cudaSuccess) return e;
+  select_kernel<G><<<n_slices, G::NT, G::SMEM, st>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st) {
-  // The dynamic shared memory opt-in is a per-device function attribute;
-  // setting it on every call is cheap and covers every device.
-  const cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(SEL_SMEM));
-  if (e != cudaSuccess) return e;
-  select_kernel<<<n_slices, NT, SEL_SMEM, st>>>(p);
-  note_launch();
-  return cudaGetLastError();
+  // The candidate span [P rounded down to 4, n_valid - W) of any slice is at
+  // most n_cap - W - (P & ~3) slots; short slices take the small geometry.
+  const int64_t span = static_cast<int64_t>(p.n_cap) - p.n_recent - (p.n_prompt & ~3);
+  if (span <= SmallGeo::KCAP) return launch_geo<SmallGeo>(p, n_slices, st);
+  return launch_geo<BigGeo>(p, n_slices, st);
 }
 
 }  // namespace tri

@@ -146,7 +146,11 @@ def test_random_stack_full_size():
     assert torch.all(kv.n_valid == B)
 
 
-def test_periodic_large_batch_full_size():
+@pytest.mark.parametrize("view", ["full_capacity", "steady_state"])
+def test_periodic_large_batch_full_size(view):
+    """Rounds run either on the whole 32768-row capacity (n_valid << n_cap)
+    or, as an engine would in steady state, on a view of capacity B + 128
+    (same storage and slice stride)."""
     w = synth.WORKLOADS["periodic_large_batch"]
     S, n_cap, P, W, B, d = w.n_slices, w.n_cap, w.n_prompt, w.n_recent, w.budget, w.head_dim
     R = w.round_rows
@@ -167,6 +171,11 @@ def test_periodic_large_batch_full_size():
     p_cur = inp.p_cur.clone()
     total_swaps, worst = 0, 0.0
     for rnd in range(w.rounds + 1):
+        if rnd == 1 and view == "steady_state":
+            cap = B + R
+            pos = pos[:, :cap].clone()
+            kv = tri.KVCache(inp.k[:, :, :, :cap], inp.v[:, :, :, :cap], kv.n_valid, pos, pos, status)
+            scores = torch.empty(S, cap, device="cuda")
         if rnd > 0:
             kn, vn = synth.append_rows(inp, rnd, R)
             inp.k[:, :, :, B:B + R] = kn
