@@ -7,9 +7,9 @@
 // earlier destination, though it may be a row that a later destination
 // overwrites (keep = {1, 2, ...}).
 //
-// One CTA owns one slice. After validating the keep list and moving the
-// positions, warp 0 moves the K rows and warp 1 the V rows, each through its
-// own 4-stage ring of 8 KB shared-memory tiles:
+// One CTA owns one slice. After validating the keep list, warp 0 moves the K
+// rows and warp 1 the V rows, each through its own 4-stage ring of 8 KB
+// shared-memory tiles, while warps 2-3 move the positions:
 //   * tile u (destination rows [u*TR, (u+1)*TR)) is gathered row by row with
 //     bulk async copies (TMA, non-tensor) completing on the stage's mbarrier;
 //   * once it has landed it is written back with ONE bulk store: past the
@@ -28,7 +28,7 @@
 namespace tri {
 namespace {
 
-constexpr int CT = 128;  // threads per CTA (validation, positions); warps 0-1 move rows
+constexpr int CT = 128;  // threads per CTA: warps 0-1 move K/V rows, warps 2-3 positions
 constexpr int CSTAGES = 4;
 constexpr int CTILE = 8192;
 constexpr size_t RING_BYTES = CSTAGES * CTILE;
@@ -54,20 +54,40 @@ __device__ __forceinline__ void move_rows(char* base, unsigned char* ring, uint6
     lo_j = max(t0, first);
     hi_j = min(t0 + TR, n_keep);
   };
-  auto gather = [&](int k) {
+  // Each lane copies rows lo_j + lane + 32 r of a tile (r < RPL); their keep
+  // entries are loaded one tile ahead so no gather waits on them.
+  constexpr int RPL = CTILE / 128 / 32;  // most rows a lane copies per tile (2)
+  int knext[RPL];
+  auto load_keep = [&](int k, int (&kv)[RPL]) {
+    int lo_j, hi_j, t0;
+    rows_of(k, lo_j, hi_j, t0);
+#pragma unroll
+    for (int r = 0; r < RPL; ++r) {
+      const int j = lo_j + lane + 32 * r;
+      kv[r] = (k < ntiles && j < hi_j) ? __ldg(keep + j) : 0;
+    }
+  };
+  auto gather = [&](int k, const int (&kv)[RPL]) {
     int lo_j, hi_j, t0;
     rows_of(k, lo_j, hi_j, t0);
     const int st = k % CSTAGES;
     if (lane == 0) mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((hi_j - lo_j) * rb));
     __syncwarp();
-    for (int j = lo_j + lane; j < hi_j; j += 32) {
-      const int kj = __ldg(keep + j);
-      bulk_g2s(ring + st * CTILE + (j - t0) * rb, base + static_cast<int64_t>(kj) * rb,
-               static_cast<uint32_t>(rb), &full[st]);
+#pragma unroll
+    for (int r = 0; r < RPL; ++r) {
+      const int j = lo_j + lane + 32 * r;
+      if (j < hi_j)
+        bulk_g2s(ring + st * CTILE + (j - t0) * rb, base + static_cast<int64_t>(kv[r]) * rb,
+                 static_cast<uint32_t>(rb), &full[st]);
     }
   };
 
-  for (int k = 0; k < min(CSTAGES - 1, ntiles); ++k) gather(k);
+  for (int k = 0; k < min(CSTAGES - 1, ntiles); ++k) {
+    int kv[RPL];
+    load_keep(k, kv);
+    gather(k, kv);
+  }
+  load_keep(CSTAGES - 1, knext);
   int k = 0;
   bool ok = true;
   for (; k < ntiles; ++k) {
@@ -84,9 +104,13 @@ __device__ __forceinline__ void move_rows(char* base, unsigned char* ring, uint6
     }
     const int kn = k + CSTAGES - 1;  // refills the stage of tile k - 1
     if (kn < ntiles) {
+      int kv[RPL];
+#pragma unroll
+      for (int r = 0; r < RPL; ++r) kv[r] = knext[r];
+      load_keep(kn + 1, knext);
       if (lane == 0) bulk_wait_read<1>();  // tile k-1's store has read its stage
       __syncwarp();
-      gather(kn);
+      gather(kn, kv);
     }
   }
   if (!ok && lane == 0) {
@@ -119,18 +143,45 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   }
   __syncthreads();
   // Validate the keep list before touching anything: ascending, keep[j] >= j,
-  // < n_cap, and -1 only as trailing padding.
-#pragma unroll 4
-  for (int j = t; j < p.budget; j += CT) {
-    const int kj = __ldg(keep + j);
-    const int prev = (j > 0) ? __ldg(keep + j - 1) : -2;
-    if (kj < 0) {
-      if (kj != -1) atomicOr(&sm.bad, 1);
-      atomicMin(&sm.n_keep, j);
+  // < n_cap, and -1 only as trailing padding. Each thread checks runs of 4
+  // entries (one 16-byte load when the list is 16-byte aligned).
+  const bool vec = (p.budget % 4 == 0) && ((reinterpret_cast<uintptr_t>(keep) & 15) == 0);
+  int bad = 0, nk = p.budget, fm = p.budget;
+  for (int j0 = 4 * t; j0 < p.budget; j0 += 4 * CT) {
+    int v[4];
+    if (vec) {
+      const int4 q = __ldg(reinterpret_cast<const int4*>(keep + j0));
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     } else {
-      if (kj < j || kj >= p.n_cap || (j > 0 && (prev < 0 || prev >= kj))) atomicOr(&sm.bad, 1);
-      if (kj != j) atomicMin(&sm.first_move, j);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = (j0 + e < p.budget) ? __ldg(keep + j0 + e) : -1;
     }
+    int prev = (j0 > 0) ? __ldg(keep + j0 - 1) : -2;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + e;
+      if (j >= p.budget) break;
+      const int kj = v[e];
+      if (kj < 0) {
+        bad |= (kj != -1);
+        nk = min(nk, j);
+      } else {
+        bad |= (kj < j || kj >= p.n_cap || (j > 0 && (prev < 0 || prev >= kj)));
+        if (kj != j) fm = min(fm, j);
+      }
+      prev = kj;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    bad |= __shfl_xor_sync(FULL_MASK, bad, o);
+    nk = min(nk, __shfl_xor_sync(FULL_MASK, nk, o));
+    fm = min(fm, __shfl_xor_sync(FULL_MASK, fm, o));
+  }
+  if (lane == 0) {
+    if (bad) atomicOr(&sm.bad, 1);
+    atomicMin(&sm.n_keep, nk);
+    atomicMin(&sm.first_move, fm);
   }
   __syncthreads();
   if (sm.bad) {
@@ -140,45 +191,49 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   const int n_keep = sm.n_keep;
   const int first = min(sm.first_move, n_keep);
 
-  {
-    int32_t* pos_out = p.pos_out + s * static_cast<int64_t>(p.n_cap);
-    const int32_t* pos_in = p.pos ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
-    if (pos_in == nullptr || pos_in != pos_out) {
-      // distinct buffers (or positions implied by the slot): a plain gather
-      for (int j = t; j < n_keep; j += CT) pos_out[j] = pos_in ? __ldg(pos_in + __ldg(keep + j)) : __ldg(keep + j);
-    } else {
-      // in place: read a chunk's sources, barrier, write it; sources of later
-      // chunks lie above every row written so far
-      for (int c0 = first; c0 < n_keep; c0 += CT * POS_PER_THREAD) {
-        int32_t v[POS_PER_THREAD];
-#pragma unroll
-        for (int e = 0; e < POS_PER_THREAD; ++e) {
-          const int j = c0 + e * CT + t;
-          v[e] = (j < n_keep) ? pos_in[__ldg(keep + j)] : 0;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < POS_PER_THREAD; ++e) {
-          const int j = c0 + e * CT + t;
-          if (j < n_keep) pos_out[j] = v[e];
-        }
-        __syncthreads();
-      }
-    }
-    if (t == 0) p.n_valid[s] = n_keep;
-  }
-  if (t >= 64 || first >= n_keep) return;
-  // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
   const int wid = t >> 5;
-  move_rows((wid == 0 ? p.k : p.v) + s * p.slice_bytes, smem + wid * RING_BYTES,
-            reinterpret_cast<uint64_t*>(smem + 2 * RING_BYTES) + wid * CSTAGES, keep, first, n_keep, p.row_bytes,
-            lane, p.dev_status);
+  if (wid < 2) {
+    // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
+    if (first < n_keep)
+      move_rows((wid == 0 ? p.k : p.v) + s * p.slice_bytes, smem + wid * RING_BYTES,
+                reinterpret_cast<uint64_t*>(smem + 2 * RING_BYTES) + wid * CSTAGES, keep, first, n_keep,
+                p.row_bytes, lane, p.dev_status);
+    return;
+  }
+  // warps 2-3 move the positions meanwhile
+  const int pt = t - 64;  // 0 .. PT-1
+  constexpr int PT = CT - 64;
+  int32_t* pos_out = p.pos_out + s * static_cast<int64_t>(p.n_cap);
+  const int32_t* pos_in = p.pos ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
+  if (pos_in == nullptr || pos_in != pos_out) {
+    // distinct buffers (or positions implied by the slot): a plain gather
+    for (int j = pt; j < n_keep; j += PT) pos_out[j] = pos_in ? __ldg(pos_in + __ldg(keep + j)) : __ldg(keep + j);
+  } else {
+    // in place: read a chunk's sources, barrier, write it; sources of later
+    // chunks lie above every row written so far
+    for (int c0 = first; c0 < n_keep; c0 += PT * POS_PER_THREAD) {
+      int32_t v[POS_PER_THREAD];
+#pragma unroll
+      for (int e = 0; e < POS_PER_THREAD; ++e) {
+        const int j = c0 + e * PT + pt;
+        v[e] = (j < n_keep) ? pos_in[__ldg(keep + j)] : 0;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(PT) : "memory");
+#pragma unroll
+      for (int e = 0; e < POS_PER_THREAD; ++e) {
+        const int j = c0 + e * PT + pt;
+        if (j < n_keep) pos_out[j] = v[e];
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(PT) : "memory");
+    }
+  }
+  if (pt == 0) p.n_valid[s] = n_keep;
 }
 
 }  // namespace
 
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st) {
-  if (p.row_bytes % 16 != 0 || p.row_bytes > CTILE) return cudaErrorInvalidValue;
+  if (p.row_bytes % 16 != 0 || p.row_bytes < 128 || p.row_bytes > CTILE) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(COMPACT_SMEM));
   if (e != cudaSuccess) return e;
