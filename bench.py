@@ -590,7 +590,7 @@ def measure_other(args, tri, synth, dev):
 
 
 KERNEL_SOURCES = {"score_kernel": "score.cu", "select_kernel": "select.cu", "compact_kernel": "compact.cu",
-                  "rand_select_kernel": "rand_select.cu"}
+                  "rand_select_kernel": "select.cu"}
 
 
 def known_traffic(workload: str, kernel: str):

@@ -159,11 +159,48 @@ def test_select_degenerate_budgets():
 
 
 def test_select_streaming_super_chunks():
-    # more than 32768 candidates: keys are re-staged per pass
+    # more candidates than the bitmaps cover: they are rebuilt piece by piece
     rng = np.random.default_rng(4)
     n_cap = 70001
     sc = (np.round(rng.normal(size=(2, n_cap)) * 64) / 64).astype(np.float32)
     _select_case(2, n_cap, 3, 5, 20000, [n_cap, 65536 + 77], sc)
+
+
+def test_select_sampled_window_full_length():
+    # 32K candidates of continuous scores: the window comes from a sample
+    rng = np.random.default_rng(11)
+    n_cap = 32768
+    sc = rng.normal(size=(4, n_cap)).astype(np.float32)
+    sc[1] += np.linspace(0, 3, n_cap, dtype=np.float32)  # a trend along the slots
+    sc[2] = np.abs(sc[2]) ** 3  # heavy tail
+    _select_case(4, n_cap, 512, 128, 4096, [n_cap, n_cap, n_cap - 5, 20000], sc)
+    _select_case(4, n_cap, 0, 0, 7, [n_cap] * 4, sc)  # tiny need
+    _select_case(4, n_cap, 8, 8, n_cap - 40, [n_cap] * 4, sc)  # keep almost all
+
+
+def test_select_threshold_ties_overflow_the_list():
+    # 6000 candidates tie at the threshold: more than the short list holds,
+    # so the exact selection over all candidates decides; lower slots win
+    rng = np.random.default_rng(12)
+    n_cap = 10000
+    sc = np.full((2, n_cap), 0.5, dtype=np.float32)
+    perm = rng.permutation(n_cap)
+    sc[0, perm[:2000]] = 2.0 + rng.random(2000)
+    sc[0, perm[2000:4000]] = -rng.random(2000)
+    sc[1] = sc[0][::-1]
+    _select_case(2, n_cap, 0, 0, 3000, [n_cap, n_cap], sc)
+
+
+def test_select_sample_misled_by_layout():
+    # every 20th slot (where a systematic sample of 2048 of 40960 candidates
+    # lands) is far below the rest, so any window drawn from those slots is
+    # wrong; the result must still be exact
+    rng = np.random.default_rng(13)
+    n_cap, P = 40960 + 64, 64
+    sc = rng.normal(size=(2, n_cap)).astype(np.float32)
+    sc[:, P + 10::20] -= 10.0
+    sc[1, P + 10::20] += 20.0  # or far above it
+    _select_case(2, n_cap, P, 0, 4000, [n_cap, n_cap], sc)
 
 
 def _compact_case(w, keep_np, pos_mode="none", seed=0):
