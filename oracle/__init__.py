@@ -26,6 +26,11 @@ Parity status of each function (what pins it, all in ``tests/test_oracle_*``):
                         uniformity statistics.
   rand_select        -- inclusion frequency, the survival-by-age law of
                         Random Attention, slot coverage across heads.
+  score_heads        -- per-query-head scores: score_series once per head;
+                        identical heads reduce to the pooled score.
+  zscore_max         -- a hand-worked two-head example in closed form,
+                        invariance under a positive affine map of any head,
+                        unit variance of every z-scored head, constant heads.
 """
 from __future__ import annotations
 
@@ -85,6 +90,8 @@ def _load():
             lib.orc_rand_u32.restype = u32
             lib.orc_rand_select.argtypes = [u64, u32, i64, i64, i64, i64, i64, i64, i64, vp]
             lib.orc_rand_select.restype = i32
+            lib.orc_zscore_max.argtypes = [vp, i64, i64, vp, vp, vp]
+            lib.orc_zscore_max.restype = None
             _lib = lib
     return _lib
 
@@ -213,3 +220,25 @@ def score_bound(k, mean_norm, style: int = ROPE_INTERLEAVED) -> np.ndarray:
     else:
         re, im = k[:, :F], k[:, F:]
     return np.hypot(re, im) @ _f64(mean_norm)
+
+
+def score_heads(k, center, mean_norm, mrl, offsets, p_cur: int, theta: float, pos=None,
+                style: int = ROPE_INTERLEAVED, norm_mode: int = NORM_WEIGHTED) -> np.ndarray:
+    """Scores of one slice under each of the G query heads that share its KV
+    head (TriAttention summary page, "Handling Grouped-Query Attention"):
+    center [G][F][2], mean_norm and mrl [G][F] are the per-query-head
+    statistics. Returns [G][n]."""
+    center = _f64(center)
+    return np.stack([score_series(k, center[g], mean_norm[g], mrl[g], offsets, p_cur, theta, pos=pos,
+                                  style=style, norm_mode=norm_mode) for g in range(center.shape[0])])
+
+
+def zscore_max(scores_g):
+    """Per-head z-score over all cached keys, then the maximum over heads
+    (TriAttention summary page, "Handling Grouped-Query Attention").
+    scores_g: [G][n]. Returns (mean [G], std [G], final [n])."""
+    s = _f64(scores_g)
+    G, n = s.shape
+    mean, std, final = np.zeros(G), np.zeros(G), np.zeros(n)
+    _load().orc_zscore_max(_ptr(s), G, n, _ptr(mean), _ptr(std), _ptr(final))
+    return mean, std, final

@@ -27,7 +27,8 @@
 // reason in the design notes of the repository):
 //   * keys are stored pre-RoPE, with a position per row (slot index when no
 //     position array is given);
-//   * the G query heads of a GQA group are pooled into one centre per KV head;
+//   * the G query heads of a GQA group are pooled into one centre per KV head
+//     (orc_zscore_max implements the paper's per-query-head alternative);
 //   * p_cur, the position of the newest cached token, is the "current query
 //     position"; a key's age is p_cur - p_i;
 //   * budget B counts every survivor, protected rows included;
@@ -39,6 +40,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <limits>
 #include <vector>
 
 namespace {
@@ -347,6 +349,40 @@ int orc_rand_select(uint64_t seed, uint32_t round, int64_t seq, int64_t layer, i
   std::sort(kept.begin(), kept.end());
   for (int64_t j = 0; j < B; ++j) keep[j] = static_cast<int32_t>(kept[j]);
   return 0;
+}
+
+// ---------------------------------------------------------------------------
+// GQA aggregation, [TA] "Handling Grouped-Query Attention (GQA)": each of the
+// G query heads that share a KV head scores every cached key with its own
+// centre statistics; per head g the mean mu_g and the standard deviation
+// sigma_g of its scores over all n cached keys turn them into z-scores, and
+// the final score of a key is the largest z-score over the G heads.
+// Readings: sigma_g is the population standard deviation (sum over n, divided
+// by n); the choice scales every head of a slice alike, so no selection can
+// depend on it. A head whose scores are all equal (sigma_g = 0) gives every
+// key a z-score of 0.
+// scores: [G][n] (head-major). Outputs mean[G], stdev[G], final_score[n].
+// ---------------------------------------------------------------------------
+void orc_zscore_max(const double* scores, int64_t G, int64_t n, double* mean, double* stdev,
+                    double* final_score) {
+  for (int64_t g = 0; g < G; ++g) {
+    const double* s = scores + g * n;
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; ++i) sum += s[i];
+    const double mu = (n > 0) ? sum / static_cast<double>(n) : 0.0;
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i) ss += (s[i] - mu) * (s[i] - mu);
+    mean[g] = mu;
+    stdev[g] = (n > 0) ? std::sqrt(ss / static_cast<double>(n)) : 0.0;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    double best = -std::numeric_limits<double>::infinity();
+    for (int64_t g = 0; g < G; ++g) {
+      const double z = (stdev[g] > 0.0) ? (scores[g * n + i] - mean[g]) / stdev[g] : 0.0;
+      if (z > best) best = z;
+    }
+    final_score[i] = best;
+  }
 }
 
 }  // extern "C"
