@@ -461,9 +461,10 @@ def run_gpu(args, w):
 
 
 def measure_other(args, tri, synth, dev):
-    """The other two 32K-token workloads, timed like the main one (CUDA
-    events around each event, first B rows restored between events):
-    Random Attention on the stack, and the large-batch periodic workload
+    """The other 32K-token workloads, timed like the main one (CUDA events
+    around each event, first B rows restored between events): Random
+    Attention on the stack, the stack with per-query-head GQA scoring
+    (z-score + max), and the large-batch periodic workload
     (its 32768-row event, then 16 rounds of +128 rows -> 2048 with explicit
     positions, the appended rows drawn outside the timed region)."""
     import numpy as np
@@ -510,6 +511,57 @@ def measure_other(args, tri, synth, dev):
                    "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
                    "algorithmic_bytes": by}
     del inp, kh, vh, kv, keep
+    torch.cuda.empty_cache()
+
+    # ---- GQA on the stack: per-query-head scores, z-score + max --------------
+    w = synth.WORKLOADS["qwen3_8b_stack"]
+    S, n, P, W, B, G = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget, w.group
+    inp = synth.make_inputs(w, dev)
+    cq = tri.calibrate_centers(inp.q, 1)  # one row per query head
+    inp.q = None
+    torch.cuda.empty_cache()
+    kh, vh = inp.k[:, :, :, :B].clone(), inp.v[:, :, :, :B].clone()
+    nv = torch.full((S,), n, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = tri.KVCache(inp.k, inp.v, nv, None, torch.empty(S, w.n_cap, dtype=torch.int32, device=dev), st)
+    scores_g = torch.empty(S, G, w.n_cap, dtype=torch.float32, device=dev)
+    stats = torch.empty(S, G, 2, dtype=torch.float32, device=dev)
+    hws = torch.empty(tri.score_heads_workspace_bytes(kv, G), dtype=torch.uint8, device=dev)
+    keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+    kms = []
+
+    def gqa_event():
+        e = [ev() for _ in range(4)]
+        e[0].record()
+        tri.score_heads(kv, cq, G, w.theta, w.offsets, inp.p_cur, scores_g, stats, workspace=hws)
+        e[1].record()
+        tri.select_topk_zmax(scores_g, stats, G, kv, P, W, B, keep)
+        e[2].record()
+        tri.compact_kv(kv, keep, B)
+        e[3].record()
+        kms.append(e)
+
+    def restore_g():
+        inp.k[:, :, :, :B].copy_(kh)
+        inp.v[:, :, :, :B].copy_(vh)
+        nv.fill_(n)
+
+    ms = timed(gqa_event, restore_g)
+    kt = [[x[0].elapsed_time(x[1]), x[1].elapsed_time(x[2]), x[2].elapsed_time(x[3])]
+          for x in kms[args.warmup:]]
+    moved = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
+    score_by = S * n * w.head_dim * w.elem_bytes  # every cached row is scored (statistics over all keys)
+    by = score_by + moved * (4 * w.head_dim * w.elem_bytes + 8)
+    assert int(st.item()) == 0
+    k_ms = [sum(x[j] for x in kt) / len(kt) for j in range(3)]
+    out["qwen3_8b_stack_gqa"] = {
+        "value": S * n / (ms / 1e3), "unit": UNIT, "ms_per_event": ms, "gbs": by / ms / 1e6,
+        "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
+        "algorithmic_bytes": by, "group": G,
+        "kernel_ms": {"score_heads": round(k_ms[0], 4), "select_zmax": round(k_ms[1], 4),
+                      "compact": round(k_ms[2], 4)},
+        "score_heads_gbs": score_by / k_ms[0] / 1e6}
+    del inp, kh, vh, kv, keep, scores_g, stats, hws
     torch.cuda.empty_cache()
 
     # ---- large-batch periodic -----------------------------------------------

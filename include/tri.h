@@ -251,6 +251,43 @@ tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_thet
                         int32_t n_recent, int32_t budget, int32_t* keep_idx, void* ws,
                         size_t ws_bytes, tri_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * GQA: one score per query head, z-score + max.
+ * [TA] "Handling Grouped-Query Attention (GQA)": the G query heads that share
+ * a KV head each score every cached key with their own statistics; per head
+ * the scores are z-normalised with their mean and standard deviation over all
+ * cached keys, and the final score of a key is the maximum over the G heads.
+ *
+ * tri_score_heads -- for every row 0 <= i < n_valid[s] of every slice and
+ * every query head g < group: scores_g[s][g][i] = S~(g)(i), the tri_score
+ * formula with the statistics of query head (layer, h * group + g), i.e. row
+ * (layer * n_kv_heads + h) * group + g of `centers` (as tri_calibrate_centers
+ * writes them with group = 1); and stats[s][g] = (mean, std) of those scores
+ * over the n_valid rows (population std: divided by n_valid; 0 and 0 for an
+ * empty slice). group: 1..8. scores_g: device [n_slices][group][n_cap] fp32
+ * (rows >= n_valid untouched); stats: device [n_slices][group][2] fp32.
+ * ws: device scratch of tri_score_heads_workspace_bytes(kv, group) bytes,
+ * 16-byte aligned (fp64 per-CTA partial sums; no initial contents needed).
+ * One pass over K computes up to four heads; larger groups take ceil(G/4)
+ * passes. The statistics are summed in a fixed order (deterministic).
+ *
+ * tri_select_topk_zmax -- tri_select_topk with the score of candidate i
+ * replaced by S_final(i) = max_g (scores_g[s][g][i] - mean_g) / std_g (a head
+ * with std 0 contributes 0), computed in fp32 as (x - mean) * (1 / std).
+ * final_scores: optional device [n_slices][n_cap]; when not NULL, S_final of
+ * every valid row is written there (the values the selection ranked).
+ * ------------------------------------------------------------------------ */
+size_t tri_score_heads_workspace_bytes(const tri_kv* kv, int32_t group);
+tri_status tri_score_heads(const tri_kv* kv, const tri_centers* centers, int32_t group,
+                           double rope_theta, tri_rope_style style, tri_norm_mode norm_mode,
+                           const int32_t* offsets, int32_t n_offsets, const int64_t* p_cur,
+                           float* scores_g, float* stats, void* ws, size_t ws_bytes,
+                           tri_stream_t stream);
+tri_status tri_select_topk_zmax(const float* scores_g, const float* stats, int32_t group,
+                                const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
+                                int32_t budget, int32_t* keep_idx, float* final_scores,
+                                tri_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

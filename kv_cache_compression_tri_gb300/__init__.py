@@ -99,6 +99,13 @@ def load_library():
         lib.tri_compress.argtypes = [kvp, ctypes.POINTER(_TriCenters), ctypes.c_double, ctypes.c_int,
                                      ctypes.c_int, vp, i32, vp, i32, i32, i32, vp, vp, ctypes.c_size_t, vp]
         lib.tri_compress.restype = ctypes.c_int
+        lib.tri_score_heads_workspace_bytes.argtypes = [kvp, i32]
+        lib.tri_score_heads_workspace_bytes.restype = ctypes.c_size_t
+        lib.tri_score_heads.argtypes = [kvp, ctypes.POINTER(_TriCenters), i32, ctypes.c_double, ctypes.c_int,
+                                        ctypes.c_int, vp, i32, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.tri_score_heads.restype = ctypes.c_int
+        lib.tri_select_topk_zmax.argtypes = [vp, vp, i32, kvp, i32, i32, i32, vp, vp, vp]
+        lib.tri_select_topk_zmax.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -277,4 +284,50 @@ def compress(kv: KVCache, centers: Centers, rope_theta: float, offsets, p_cur: t
                                             norm_mode, ctypes.cast(offs, ctypes.c_void_p), len(offsets),
                                             p_cur.data_ptr(), n_prompt, n_recent, budget, keep.data_ptr(),
                                             workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return keep
+
+
+def score_heads_workspace_bytes(kv: KVCache, group: int) -> int:
+    kvs = kv._abi()
+    return int(load_library().tri_score_heads_workspace_bytes(ctypes.byref(kvs), group))
+
+
+def score_heads(kv: KVCache, centers: Centers, group: int, rope_theta: float, offsets, p_cur: torch.Tensor,
+                scores_g: torch.Tensor, stats: torch.Tensor, workspace: torch.Tensor | None = None,
+                style: int = ROPE_INTERLEAVED, norm_mode: int = NORM_WEIGHTED, stream=None):
+    """Per-query-head scores [S, group, n_cap] of every valid row and their
+    per-head (mean, std) [S, group, 2] (tri_score_heads). `centers` holds one
+    row per query head (calibrate_centers with group=1)."""
+    lib = load_library()
+    offs = (ctypes.c_int32 * len(offsets))(*[int(o) for o in offsets])
+    assert p_cur.dtype == torch.int64 and p_cur.is_cuda
+    assert scores_g.dtype == torch.float32 and scores_g.is_contiguous()
+    assert scores_g.numel() == kv.n_slices * group * kv.k.shape[3]
+    assert stats.dtype == torch.float32 and stats.is_contiguous() and stats.numel() == kv.n_slices * group * 2
+    kvs, cs = kv._abi(), centers._abi()
+    need = int(lib.tri_score_heads_workspace_bytes(ctypes.byref(kvs), group))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=kv.k.device)
+    assert workspace.numel() >= need
+    _check("tri_score_heads", lib.tri_score_heads(
+        ctypes.byref(kvs), ctypes.byref(cs), group, float(rope_theta), style, norm_mode,
+        ctypes.cast(offs, ctypes.c_void_p), len(offsets), p_cur.data_ptr(), scores_g.data_ptr(),
+        stats.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return scores_g, stats
+
+
+def select_topk_zmax(scores_g: torch.Tensor, stats: torch.Tensor, group: int, kv: KVCache, n_prompt: int,
+                     n_recent: int, budget: int, keep: torch.Tensor, final_scores: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Protected top-budget keep lists ranked by the GQA z-score maximum
+    (tri_select_topk_zmax); optionally writes the final scores [S, n_cap]."""
+    lib = load_library()
+    assert keep.dtype == torch.int32 and keep.is_contiguous() and keep.numel() == kv.n_slices * budget
+    if final_scores is not None:
+        assert final_scores.dtype == torch.float32 and final_scores.is_contiguous()
+        assert final_scores.numel() == kv.n_slices * kv.k.shape[3]
+    kvs = kv._abi()
+    _check("tri_select_topk_zmax", lib.tri_select_topk_zmax(
+        scores_g.data_ptr(), stats.data_ptr(), group, ctypes.byref(kvs), n_prompt, n_recent, budget,
+        keep.data_ptr(), _ptr(final_scores), _stream(stream)))
     return keep

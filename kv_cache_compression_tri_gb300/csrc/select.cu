@@ -1,7 +1,8 @@
 // select.cu -- per-slice budgeted selection, one CTA per slice.
 //
 // Keep [0, P) U top-(B-P-W) candidates U [n-W, n), ascending; among equal
-// keys the lower slot wins. Two key sources share the kernel:
+// keys the lower slot wins. Three key sources share the kernel (the third,
+// ZMaxKeys, ranks by the GQA z-score maximum, below):
 //   * scores -- TriAttention paper summary, "Retention and eviction" (top-B
 //     by score); Random Attention, Eq. 2 (top-K with the prompt forced in):
 //     the key of candidate i is the order-preserving u32 of its fp32 score;
@@ -212,6 +213,66 @@ __device__ __forceinline__ void block_minmax(SSmem& sm, uint32_t& kmin, uint32_t
   __syncthreads();  // wmin / wmax may be rewritten by the next call
 }
 
+// Window from a systematic sample of the candidates: candidate P + floor((2j
+// + 1) m / (2 NSAMPLE)) for j < NSAMPLE, whose key key_of(slot) gives. The
+// sample keys of ranks r* -+ SAMPLE_SD sd bound [t_lo, t_hi] (r* = need
+// NSAMPLE / m, sd its binomial standard deviation).
+template <class KeyOf>
+__device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const KeyOf& key_of, uint32_t& t_lo,
+                               uint32_t& t_hi) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  uint32_t sk[SPT];
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int r = 0; r < SPT; ++r) {
+    const int j = t + NT * r;
+    const int slot = c.P + static_cast<int>(((2LL * j + 1) * m) / (2LL * NSAMPLE));
+    sk[r] = key_of(slot);
+    kmin = min(kmin, sk[r]);
+    kmax = max(kmax, sk[r]);
+  }
+  block_minmax(sm, kmin, kmax);
+  // sample ranks (1 = largest) that bracket the need-th largest candidate
+  const double rho = static_cast<double>(need) / m;
+  const double rs = rho * NSAMPLE, sd = sqrt(NSAMPLE * rho * (1.0 - rho));
+  const int ra = static_cast<int>(floor(rs - SAMPLE_SD * sd - 1.0));
+  const int rb = static_cast<int>(ceil(rs + SAMPLE_SD * sd + 1.0));
+  Radix A, B;
+  const bool want_a = ra >= 1, want_b = rb <= NSAMPLE;
+  A.start(kmin, kmax, static_cast<unsigned>(max(ra, 1)));
+  B.start(kmin, kmax, static_cast<unsigned>(min(rb, NSAMPLE)));
+  A.done |= !want_a;
+  B.done |= !want_b;
+  // Refine both ranks together until their bins hold at most 4 sample
+  // keys (or the full key is known): t_hi is the top of A's bin, so fewer
+  // than ra sample keys lie above it; t_lo the bottom of B's bin, so at
+  // least rb lie at or above it.
+  while (!(A.done && B.done)) {
+    sm.hist[0][t] = 0u;
+    sm.hist[1][t] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < SPT; ++r) {
+      if (!A.done && A.matches(sk[r])) atomicAdd(&sm.hist[0][A.digit(sk[r])], 1u);
+      if (!B.done && B.matches(sk[r])) atomicAdd(&sm.hist[1][B.digit(sk[r])], 1u);
+    }
+    __syncthreads();
+    if (w == 0 && !A.done) pick_bin(sm, sm.hist[0], A.need, lane, 0);
+    if (w == 1 && !B.done) pick_bin(sm, sm.hist[1], B.need, lane, 1);
+    __syncthreads();
+    if (!A.done) {
+      const unsigned cnt = A.take(sm, 0);
+      if (cnt <= 4u || A.shift == 0) A.done = true; else A.next_digit();
+    }
+    if (!B.done) {
+      const unsigned cnt = B.take(sm, 1);
+      if (cnt <= 4u || B.shift == 0) B.done = true; else B.next_digit();
+    }
+  }
+  t_hi = want_a ? (A.prefix | ((1u << A.shift) - 1u) | ~A.mask) : 0xffffffffu;
+  t_lo = want_b ? (B.prefix & B.mask) : 0u;
+}
+
 // ---- key sources --------------------------------------------------------------
 
 // fp32 scores [S][n_cap]; keys of slots outside [P, end) read as 0.
@@ -244,60 +305,12 @@ struct ScoreKeys {
     for (int e = 0; e < 4; ++e) k[e] = in_range(i0 + e, P, end) ? score_key(x[e], nan) : 0u;
     return make_uint4(k[0], k[1], k[2], k[3]);
   }
-  // Window from a systematic sample: candidate P + floor((2j+1) m / (2 NSAMPLE)).
   __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
-    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    uint32_t sk[SPT];
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    bool ignored = false;  // NaN is flagged by the full pass
-#pragma unroll
-    for (int r = 0; r < SPT; ++r) {
-      const int j = t + NT * r;
-      const int slot = c.P + static_cast<int>(((2LL * j + 1) * m) / (2LL * NSAMPLE));
-      sk[r] = score_key(__ldcg(row + slot), ignored);
-      kmin = min(kmin, sk[r]);
-      kmax = max(kmax, sk[r]);
-    }
-    block_minmax(sm, kmin, kmax);
-    // sample ranks (1 = largest) that bracket the need-th largest candidate
-    const double rho = static_cast<double>(need) / m;
-    const double rs = rho * NSAMPLE, sd = sqrt(NSAMPLE * rho * (1.0 - rho));
-    const int ra = static_cast<int>(floor(rs - SAMPLE_SD * sd - 1.0));
-    const int rb = static_cast<int>(ceil(rs + SAMPLE_SD * sd + 1.0));
-    Radix A, B;
-    const bool want_a = ra >= 1, want_b = rb <= NSAMPLE;
-    A.start(kmin, kmax, static_cast<unsigned>(max(ra, 1)));
-    B.start(kmin, kmax, static_cast<unsigned>(min(rb, NSAMPLE)));
-    A.done |= !want_a;
-    B.done |= !want_b;
-    // Refine both ranks together until their bins hold at most 4 sample
-    // keys (or the full key is known): t_hi is the top of A's bin, so fewer
-    // than ra sample keys lie above it; t_lo the bottom of B's bin, so at
-    // least rb lie at or above it.
-    while (!(A.done && B.done)) {
-      sm.hist[0][t] = 0u;
-      sm.hist[1][t] = 0u;
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < SPT; ++r) {
-        if (!A.done && A.matches(sk[r])) atomicAdd(&sm.hist[0][A.digit(sk[r])], 1u);
-        if (!B.done && B.matches(sk[r])) atomicAdd(&sm.hist[1][B.digit(sk[r])], 1u);
-      }
-      __syncthreads();
-      if (w == 0 && !A.done) pick_bin(sm, sm.hist[0], A.need, lane, 0);
-      if (w == 1 && !B.done) pick_bin(sm, sm.hist[1], B.need, lane, 1);
-      __syncthreads();
-      if (!A.done) {
-        const unsigned cnt = A.take(sm, 0);
-        if (cnt <= 4u || A.shift == 0) A.done = true; else A.next_digit();
-      }
-      if (!B.done) {
-        const unsigned cnt = B.take(sm, 1);
-        if (cnt <= 4u || B.shift == 0) B.done = true; else B.next_digit();
-      }
-    }
-    t_hi = want_a ? (A.prefix | ((1u << A.shift) - 1u) | ~A.mask) : 0xffffffffu;
-    t_lo = want_b ? (B.prefix & B.mask) : 0u;
+    const float* r = row;
+    sampled_window(sm, c, need, m, [r](int slot) {
+      bool ignored = false;  // NaN is flagged by the full pass
+      return score_key(__ldcg(r + slot), ignored);
+    }, t_lo, t_hi);
   }
 };
 
@@ -329,6 +342,75 @@ struct DrawKeys {
     __syncthreads();
     t_lo = sm.t_lo;
     t_hi = sm.t_hi;
+  }
+};
+
+// Final GQA scores, TriAttention paper summary, "Handling Grouped-Query
+// Attention": the key of candidate i is the order-preserving u32 of
+// max_g (S~(g)(i) - mean_g) / std_g over the group's G query heads, formed on
+// the fly from the per-head scores [S][G][n_cap] and statistics [S][G][2].
+template <int G>
+struct ZMaxKeys {
+  static constexpr int U = 1;
+  const float* base;  // this slice's head 0 row
+  int64_t n_cap;
+  float mu[G], inv[G];
+  bool vec;
+
+  __device__ static ZMaxKeys make(const SelectParams& p, const Ctx& c, int, int, int) {
+    ZMaxKeys k;
+    k.n_cap = p.n_cap;
+    k.base = p.scores + c.s * G * k.n_cap;
+    k.vec = (reinterpret_cast<uintptr_t>(k.base) & 15) == 0 && (p.n_cap & 3) == 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      k.mu[g] = p.stats[(c.s * G + g) * 2];
+      k.inv[g] = head_inv_std(p.stats[(c.s * G + g) * 2 + 1]);
+    }
+    return k;
+  }
+  __device__ __forceinline__ float final_score(int slot) const {
+    float best = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float z = head_z(__ldcg(base + g * n_cap + slot), mu[g], inv[g]);
+      best = (g == 0) ? z : fmaxf(best, z);
+    }
+    return best;
+  }
+  __device__ __forceinline__ uint4 fetch(int i0, int P, int end, bool& nan) const {
+    float best[4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float* row = base + g * n_cap;
+      float x[4];
+      if (vec && i0 + 3 < end) {
+        const float4 f = __ldcg(reinterpret_cast<const float4*>(row + i0));
+        x[0] = f.x;
+        x[1] = f.y;
+        x[2] = f.z;
+        x[3] = f.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = (i0 + e < end) ? __ldcg(row + i0 + e) : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float z = head_z(x[e], mu[g], inv[g]);
+        best[e] = (g == 0) ? z : fmaxf(best[e], z);
+      }
+    }
+    uint32_t k[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) k[e] = in_range(i0 + e, P, end) ? score_key(best[e], nan) : 0u;
+    return make_uint4(k[0], k[1], k[2], k[3]);
+  }
+  __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
+    const ZMaxKeys& self = *this;
+    sampled_window(sm, c, need, m, [&self](int slot) {
+      bool ignored = false;
+      return score_key(self.final_score(slot), ignored);
+    }, t_lo, t_hi);
   }
 };
 
@@ -622,6 +704,20 @@ cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st) 
 
 cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st) {
   return launch_src<DrawKeys>(p, n_slices, st);
+}
+
+cudaError_t launch_select_zmax(const SelectParams& p, int n_slices, cudaStream_t st) {
+  switch (p.group) {
+    case 1: return launch_src<ZMaxKeys<1>>(p, n_slices, st);
+    case 2: return launch_src<ZMaxKeys<2>>(p, n_slices, st);
+    case 3: return launch_src<ZMaxKeys<3>>(p, n_slices, st);
+    case 4: return launch_src<ZMaxKeys<4>>(p, n_slices, st);
+    case 5: return launch_src<ZMaxKeys<5>>(p, n_slices, st);
+    case 6: return launch_src<ZMaxKeys<6>>(p, n_slices, st);
+    case 7: return launch_src<ZMaxKeys<7>>(p, n_slices, st);
+    case 8: return launch_src<ZMaxKeys<8>>(p, n_slices, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace tri

@@ -128,6 +128,17 @@ tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layer
 namespace tri {
 namespace {
 
+// Rows per CTA of the score kernels: ~512 KB of keys (32 tiles), fewer for
+// small caches; and the CTAs per slice.
+void score_tiling(const tri_kv* kv, int32_t& rows_per_cta, int32_t& tiles_per_slice) {
+  const ScoreGeometry g = score_geometry(kv->dtype, kv->head_dim);
+  int rpc = 32 * g.tile_rows;
+  const int cap_rows = (kv->n_cap + g.tile_rows - 1) / g.tile_rows * g.tile_rows;
+  if (cap_rows < rpc) rpc = cap_rows;
+  rows_per_cta = rpc;
+  tiles_per_slice = static_cast<int32_t>((kv->n_cap + rpc - 1) / rpc);
+}
+
 // Shared by tri_score and tri_compress: argument checks and the score
 // kernel's parameter block (host fp64 per-band constants).
 tri_status prepare_score(const tri_kv* kv, const tri_centers* c, double rope_theta, tri_rope_style style,
@@ -177,12 +188,7 @@ tri_status prepare_score(const tri_kv* kv, const tri_centers* c, double rope_the
   p.n_prompt = n_prompt;
   p.n_recent = n_recent;
   p.norm_mode = norm_mode;
-  // ~512 KB of keys per CTA (32 tiles), fewer for small caches.
-  int rpc = 32 * g.tile_rows;
-  const int cap_rows = (kv->n_cap + g.tile_rows - 1) / g.tile_rows * g.tile_rows;
-  if (cap_rows < rpc) rpc = cap_rows;
-  p.rows_per_cta = rpc;
-  p.tiles_per_slice = static_cast<int32_t>((kv->n_cap + rpc - 1) / rpc);
+  score_tiling(kv, p.rows_per_cta, p.tiles_per_slice);
   if (slices_of(kv) * p.tiles_per_slice > 0x7fffffff) return TRI_ERR_INVALID_ARG;
   return TRI_OK;
 }
@@ -304,6 +310,67 @@ tri_status tri_compact_kv(const tri_kv* kv, const int32_t* keep_idx, int32_t bud
   if (!kv->pos_out) return TRI_ERR_INVALID_ARG;
   if (!keep_idx || !aligned(keep_idx, 4) || budget < 1 || budget > kv->n_cap) return TRI_ERR_INVALID_ARG;
   const cudaError_t e = launch_compact(compact_params(kv, keep_idx, budget), static_cast<int>(slices_of(kv)), stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+size_t tri_score_heads_workspace_bytes(const tri_kv* kv, int32_t group) {
+  if (check_kv(kv, false) != TRI_OK || group < 1 || group > MAX_GROUP) return 0;
+  int32_t rpc, tiles;
+  score_tiling(kv, rpc, tiles);
+  return static_cast<size_t>(slices_of(kv)) * tiles * group * 3 * sizeof(double);
+}
+
+tri_status tri_score_heads(const tri_kv* kv, const tri_centers* centers, int32_t group, double rope_theta,
+                           tri_rope_style style, tri_norm_mode norm_mode, const int32_t* offsets,
+                           int32_t n_offsets, const int64_t* p_cur, float* scores_g, float* stats,
+                           void* ws, size_t ws_bytes, tri_stream_t stream) {
+  if (group < 1 || group > MAX_GROUP) return TRI_ERR_INVALID_ARG;
+  if (!stats || !aligned(stats, 8)) return TRI_ERR_INVALID_ARG;
+  ScoreParams p;
+  tri_status st = prepare_score(kv, centers, rope_theta, style, norm_mode, offsets, n_offsets, p_cur, 0, 0,
+                                scores_g, false, p);
+  if (st != TRI_OK) return st;
+  const size_t need = tri_score_heads_workspace_bytes(kv, group);
+  if (need == 0 || ws_bytes < need || !ws || !aligned(ws, 16)) return TRI_ERR_INVALID_ARG;
+  p.scores = nullptr;
+  p.scores_g = scores_g;
+  p.partials = static_cast<double*>(ws);
+  p.group = group;
+  const int n_slices = static_cast<int>(slices_of(kv));
+  for (int h0 = 0; h0 < group; h0 += MAX_HEADS_PER_LAUNCH) {
+    p.head0 = h0;
+    const int nh = group - h0 < MAX_HEADS_PER_LAUNCH ? group - h0 : MAX_HEADS_PER_LAUNCH;
+    const cudaError_t e = launch_score_heads(p, nh, kv->dtype, kv->head_dim, style, kv->pos != nullptr,
+                                             n_slices, stream);
+    if (e != cudaSuccess) return TRI_ERR_CUDA;
+  }
+  const cudaError_t e = launch_heads_stats(p.partials, stats, n_slices, p.tiles_per_slice, group, stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status tri_select_topk_zmax(const float* scores_g, const float* stats, int32_t group, const tri_kv* kv,
+                                int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                                float* final_scores, tri_stream_t stream) {
+  if (!kv) return TRI_ERR_INVALID_ARG;
+  if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
+  if (!kv->n_valid || !aligned(kv->n_valid, 4)) return TRI_ERR_INVALID_ARG;
+  if (group < 1 || group > MAX_GROUP) return TRI_ERR_INVALID_ARG;
+  if (!scores_g || !aligned(scores_g, 4) || !stats || !aligned(stats, 8)) return TRI_ERR_INVALID_ARG;
+  if (!keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
+  if (final_scores && !aligned(final_scores, 4)) return TRI_ERR_INVALID_ARG;
+  tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
+  if (slices_of(kv) > 0x7fffffff) return TRI_ERR_INVALID_ARG;
+  const int n_slices = static_cast<int>(slices_of(kv));
+  if (final_scores) {
+    const cudaError_t e = launch_zmax_scores(scores_g, stats, kv->n_valid, final_scores, n_slices, kv->n_cap,
+                                             group, stream);
+    if (e != cudaSuccess) return TRI_ERR_CUDA;
+  }
+  SelectParams p = select_params(scores_g, kv, n_prompt, n_recent, budget, keep_idx);
+  p.stats = stats;
+  p.group = group;
+  const cudaError_t e = launch_select_zmax(p, n_slices, stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 

@@ -173,6 +173,13 @@ __device__ __forceinline__ uint32_t score_key(float x, bool& nan) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// z-score of one query head's score, from the head's mean and 1/std over the
+// slice (TriAttention paper summary, "Handling Grouped-Query Attention"); a
+// head whose scores are all equal (std 0) gives 0. Every kernel that ranks or
+// reports z-scores uses these two, so they agree bit for bit.
+__device__ __forceinline__ float head_inv_std(float sd) { return sd > 0.f ? 1.0f / sd : 0.f; }
+__device__ __forceinline__ float head_z(float v, float mu, float inv) { return __fmul_rn(__fsub_rn(v, mu), inv); }
+
 // ---------------------------------------------------------------------------
 // Kernel parameter blocks (passed by value).
 // ---------------------------------------------------------------------------
@@ -200,6 +207,11 @@ struct ScoreParams {
   float step_im[MAX_BANDS];
   float jump_re[MAX_BANDS];   // e^{-i omega_f * (positions skipped between tiles)}
   float jump_im[MAX_BANDS];
+  // per-query-head scoring (GQA): centre rows are (layer * H + h) * group + g
+  int32_t group;     // query heads per KV head
+  int32_t head0;     // first query head (within the group) of this launch
+  float* scores_g;   // [S][group][n_cap]
+  double* partials;  // [S][tiles_per_slice][group][3]: sum, sum of squares, rows
 };
 
 struct SelectParams {
@@ -211,6 +223,9 @@ struct SelectParams {
   int32_t n_layers, n_kv_heads;
   uint64_t seed;
   uint32_t round;
+  // z-score + max source: per-head scores [S][group][n_cap], stats [S][group][2]
+  const float* stats;
+  int32_t group;
 };
 
 struct CompactParams {
@@ -251,6 +266,18 @@ struct ScoreGeometry {
 };
 ScoreGeometry score_geometry(tri_dtype dt, int head_dim);
 cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st);
+// Per-query-head scores and per-CTA statistics partials, heads [head0, head0 +
+// n_heads) of every group; then the per-(slice, head) mean and standard
+// deviation; then (optional) the z-score maximum of every valid row.
+constexpr int MAX_HEADS_PER_LAUNCH = 4;
+constexpr int MAX_GROUP = 8;
+cudaError_t launch_score_heads(const ScoreParams& p, int n_heads, tri_dtype dt, int head_dim,
+                               tri_rope_style style, bool explicit_pos, int n_slices, cudaStream_t st);
+cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slices, int tiles_per_slice,
+                               int group, cudaStream_t st);
+cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid,
+                               float* out, int n_slices, int n_cap, int group, cudaStream_t st);
+cudaError_t launch_select_zmax(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_calibrate(const CalibParams& p, tri_dtype dt, int head_dim,
