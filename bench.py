@@ -291,7 +291,8 @@ def workload_config(w, path: str = "separate") -> dict:
         "rope_theta": w.theta, "storage": "bf16" if w.elem_bytes == 2 else "f32",
         "path": ("rand_evict + tri_compact_kv" if w.random else
                  ("tri_compress (score, select, compact in one call)" if path == "compress" else
-                  "tri_score + tri_select_topk + tri_compact_kv")),
+                  ("tri_score_heads + tri_select_topk_zmax + tri_compact_kv (GQA z-score + max, group %d)"
+                   % w.group if path == "gqa" else "tri_score + tri_select_topk + tri_compact_kv"))),
         "parallelism": "one cache batch per GPU (weak scaling)",
     }
 
@@ -321,8 +322,10 @@ def run_gpu(args, w):
     d, e = w.head_dim, w.elem_bytes
     inp = synth.make_inputs(w, dev)
     centers = None
+    gqa = (args.path == "gqa") and not w.random
     if not w.random:
-        centers = tri.calibrate_centers(inp.q, w.group)
+        # the GQA path keeps one centre per query head
+        centers = tri.calibrate_centers(inp.q, 1 if gqa else w.group)
         inp.q = None
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -334,7 +337,12 @@ def run_gpu(args, w):
     pos_out = torch.empty(S, w.n_cap, dtype=torch.int32, device=dev)
     kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status)
     fused = (args.path == "compress") and not w.random
-    scores = None if fused else torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    scores = None if (fused or gqa) else torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    if gqa:
+        G = w.group
+        scores_g = torch.empty(S, G, w.n_cap, dtype=torch.float32, device=dev)
+        stats = torch.empty(S, G, 2, dtype=torch.float32, device=dev)
+        hws = torch.empty(tri.score_heads_workspace_bytes(kv, G), dtype=torch.uint8, device=dev)
     keep = torch.empty(S, B, dtype=torch.int32, device=dev)
     cws = torch.empty(tri.compress_workspace_bytes(kv), dtype=torch.uint8, device=dev) if fused else None
     stream = torch.cuda.current_stream()
@@ -360,6 +368,11 @@ def run_gpu(args, w):
             if rec: rec[0].record(stream)
             tri.rand_evict(kv, 0, 0, P, W, B, keep)
             if rec: rec[1].record(stream)
+        elif gqa:
+            if rec: rec[0].record(stream)
+            tri.score_heads(kv, centers, G, w.theta, w.offsets, inp.p_cur, scores_g, stats, workspace=hws)
+            if rec: rec[1].record(stream)
+            tri.select_topk_zmax(scores_g, stats, G, kv, P, W, B, keep)
         else:
             if rec: rec[0].record(stream)
             tri.score(kv, centers, w.theta, w.offsets, inp.p_cur, scores, n_prompt=P, n_recent=W)
@@ -412,7 +425,7 @@ def run_gpu(args, w):
     agg = aggregate(S * n, ws, max_sec, args.steps)
 
     # algorithmic bytes
-    cand_rows = S * (n - P - W)
+    cand_rows = S * n if gqa else S * (n - P - W)  # GQA statistics cover every cached row
     score_bytes = 0 if w.random else cand_rows * d * e
     compact_bytes = moved * (4 * d * e + 8)
     step_bytes = score_bytes + compact_bytes
@@ -421,7 +434,7 @@ def run_gpu(args, w):
     if w.random:
         dom_name, dom_ms, dom_bytes = "compact_kernel", mean(k3_ms), compact_bytes
     else:
-        dom_name, dom_ms, dom_bytes = "score_kernel", mean(k1_ms), score_bytes
+        dom_name, dom_ms, dom_bytes = ("score_heads_kernel" if gqa else "score_kernel"), mean(k1_ms), score_bytes
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = known_traffic(w.name, dom_name)
     result = {
@@ -435,7 +448,7 @@ def run_gpu(args, w):
         "hbm_frac_of_8tbs": step_bytes / (dev_sec / args.steps) / 1e9 / 8000.0,
         "algorithmic_bytes_per_step": step_bytes,
         "kernel_ms": ({"compress": round(mean(k1_ms), 4)} if fused else
-                      {"score" if not w.random else "rand_select": round(mean(k1_ms), 4),
+                      {("score_heads" if gqa else "score") if not w.random else "rand_select": round(mean(k1_ms), 4),
                        "select": round(mean(k2_ms), 4), "compact": round(mean(k3_ms), 4)}),
         "moved_rows_per_step": moved,
         "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -447,7 +460,7 @@ def run_gpu(args, w):
     }
     del scores, cws
     torch.cuda.empty_cache()
-    if not args.no_e2e:
+    if not args.no_e2e and not gqa:
         result["e2e"] = run_e2e(args, w, tri, synth, inp, centers, dev, stream)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, w)
@@ -642,6 +655,7 @@ def measure_other(args, tri, synth, dev):
 
 
 KERNEL_SOURCES = {"score_kernel": "score.cu", "select_kernel": "select.cu", "compact_kernel": "compact.cu",
+                  "score_heads_kernel": "score_heads.cu",
                   "rand_select_kernel": "select.cu"}
 
 
@@ -753,9 +767,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gpu", "reference", "ours"], default="gpu")
     ap.add_argument("--workload", default="qwen3_8b_stack")
-    ap.add_argument("--path", choices=["separate", "compress"], default="separate",
+    ap.add_argument("--path", choices=["separate", "compress", "gqa"], default="separate",
                     help="separate: tri_score + tri_select_topk + tri_compact_kv (per-kernel events); "
-                         "compress: the single tri_compress call")
+                         "compress: the single tri_compress call; gqa: per-query-head scores, "
+                         "z-score + max selection, compaction")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other 32K-token workloads")

@@ -27,7 +27,7 @@
 //     partial sums are reduced across the TPK lanes with a transposed
 //     butterfly that leaves consecutive scores in consecutive lanes.
 // Every wait on a tile is bounded in wall-clock time; a timeout records
-// TRI_DEV_TIMEOUT, drains the copies in flight and leaves the tile unscored.
+// TRI_DEV_TIMEOUT, drains the copies in flight and leaves the rest unscored.
 
 #include <cuda_runtime.h>
 
@@ -70,8 +70,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   constexpr int ROW_BYTES = G::ROW_BYTES, TILE_ROWS = G::TILE_ROWS, RPW = G::RPW, STEPS = G::STEPS;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
-  volatile int* failed = reinterpret_cast<volatile int*>(full + STAGES);
+  RingCtrl& rc = *reinterpret_cast<RingCtrl*>(smem + RING_BYTES);
 
   const int64_t s = blockIdx.x / p.tiles_per_slice;
   const int ct = blockIdx.x % p.tiles_per_slice;
@@ -92,16 +91,11 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   auto issue = [&](int u) {
     const int rows = min(TILE_ROWS, c1 - c0 - u * TILE_ROWS);
     const uint32_t bytes = static_cast<uint32_t>(rows * ROW_BYTES);
-    uint64_t* bar = &full[u % STAGES];
+    uint64_t* bar = &rc.full[u % STAGES];
     mbar_arrive_expect_tx(bar, bytes);
     bulk_g2s(ring + (u % STAGES) * TILE_BYTES, src + static_cast<int64_t>(u) * TILE_BYTES, bytes, bar);
   };
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int st = 0; st < STAGES; ++st) mbar_init(&full[st], 1);
-    *failed = 0;
-    mbar_init_fence();
-  }
+  if (threadIdx.x == 0) ring_init(rc, ntiles);
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int u = 0; u < min(STAGES, ntiles); ++u) issue(u);
@@ -155,14 +149,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   float* out = p.scores + s * static_cast<int64_t>(p.n_cap);
   const int32_t* pos = EXPLICIT_POS ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
 
-  int t = 0;
-  for (; t < ntiles; ++t) {
+  for (int t = 0; t < ntiles; ++t) {
     const int st = t % STAGES;
-    bool ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((t / STAGES) & 1));
-    ok = __all_sync(FULL_MASK, ok);
-    if (!ok) {
-      if (lane == 0) *failed = 1;
-    } else {
+    // a warp whose wait timed out still reaches the barrier below
+    if (ring_wait(rc, t, lane)) {
       const unsigned char* tile = ring + st * TILE_BYTES;
       const int rbase = warp * RPW + kq;  // row within the tile of this lane's first key
       int pp[STEPS];
@@ -222,20 +212,19 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
       const int r = c0 + t * TILE_ROWS + rbase + idx * KPW;
       if ((c % (TPK / STEPS)) == 0 && r < c1) __stcs(out + r, v);
     }
-    __syncthreads();  // the whole CTA is done with stage st
-    if (*failed) break;
+    // This kernel is near its issue limit and keeps its warps in step: the
+    // whole CTA finishes a stage before thread 0 refills it (measured a
+    // little faster here than the per-warp release the heads kernel uses).
+    __syncthreads();
+    if (ring_failed(rc)) break;
     if (threadIdx.x == 0 && t + STAGES < ntiles) {
       fence_proxy_async_smem();
       issue(t + STAGES);
+      rc.issued = t + STAGES + 1;
     }
   }
-  if (t < ntiles && threadIdx.x == 0) {
-    // A wait timed out: report it and let the copies already in flight land
-    // before the CTA's shared memory is released.
-    set_status(p.dev_status, TRI_DEV_TIMEOUT);
-    for (int u = t; u < min(ntiles, t + STAGES); ++u)
-      (void)mbar_wait_bounded(&full[u % STAGES], static_cast<uint32_t>((u / STAGES) & 1));
-  }
+  __syncthreads();
+  ring_drain(rc, p.dev_status);
 }
 
 template <typename T, int D, int STYLE, bool EXPLICIT_POS>

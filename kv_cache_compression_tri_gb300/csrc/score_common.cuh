@@ -16,7 +16,79 @@ constexpr int SCORE_THREADS = 256;
 constexpr int SCORE_WARPS = SCORE_THREADS / 32;
 constexpr int STAGES = 4;
 constexpr int TILE_BYTES = 16384;
-constexpr size_t SCORE_SMEM = STAGES * TILE_BYTES + STAGES * sizeof(uint64_t) + 16;
+constexpr size_t RING_BYTES = static_cast<size_t>(STAGES) * TILE_BYTES;
+
+// Control block of a CTA's tile ring, placed after the tiles.
+struct RingCtrl {
+  uint64_t full[STAGES];      // the stage's tile has landed (bulk copy completion)
+  unsigned consumed[STAGES];  // warps done with the stage's current tile
+  int failed;                 // a wait timed out
+  int issued;                 // tiles issued so far
+};
+constexpr size_t SCORE_SMEM = RING_BYTES + (sizeof(RingCtrl) + 15) / 16 * 16;
+
+// The ring: consecutive TILE_BYTES chunks of the CTA's rows, each filled by
+// one bulk async copy (TMA, non-tensor) that completes on its stage's
+// mbarrier. Warps move through it independently: a warp waits only for the
+// tile it needs (bounded in wall-clock time), and the last warp to finish a
+// stage refills it -- no CTA barrier per tile. The release counter's atomics,
+// fenced at CTA scope, order every warp's shared-memory reads of the stage
+// before the refill, which is issued after a generic-to-async proxy fence.
+
+// Thread 0, before the CTA's first barrier.
+__device__ __forceinline__ void ring_init(RingCtrl& rc, int ntiles) {
+#pragma unroll
+  for (int st = 0; st < STAGES; ++st) {
+    mbar_init(&rc.full[st], 1);
+    rc.consumed[st] = 0u;
+  }
+  rc.failed = 0;
+  rc.issued = min(STAGES, ntiles);
+  mbar_init_fence();
+}
+
+__device__ __forceinline__ bool ring_failed(const RingCtrl& rc) {
+  return *reinterpret_cast<const volatile int*>(&rc.failed) != 0;
+}
+
+// Wait for tile t (warp-uniform result); a timeout marks the CTA failed.
+__device__ __forceinline__ bool ring_wait(RingCtrl& rc, int t, int lane) {
+  bool ok = mbar_wait_bounded(&rc.full[t % STAGES], static_cast<uint32_t>((t / STAGES) & 1));
+  ok = __all_sync(FULL_MASK, ok);
+  if (!ok && lane == 0) atomicExch(&rc.failed, 1);
+  return ok;
+}
+
+// A warp is done with tile t; the CTA's last warp to get there issues tile
+// t + STAGES into the stage (issue(u) starts the copy of tile u).
+template <class Issue>
+__device__ __forceinline__ void ring_release(RingCtrl& rc, int t, int ntiles, int lane, const Issue& issue) {
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    if (atomicAdd(&rc.consumed[t % STAGES], 1u) == SCORE_WARPS - 1) {
+      atomicExch(&rc.consumed[t % STAGES], 0u);
+      __threadfence_block();
+      if (t + STAGES < ntiles) {
+        fence_proxy_async_smem();
+        issue(t + STAGES);
+        atomicMax(&rc.issued, t + STAGES + 1);
+      }
+    }
+  }
+}
+
+// After the CTA's last barrier: on a timeout, record it and let the copies
+// in flight land before the shared memory is released (the last tile issued
+// into each stage is the newest one there).
+__device__ __forceinline__ void ring_drain(RingCtrl& rc, int32_t* dev_status) {
+  if (threadIdx.x == 0 && ring_failed(rc)) {
+    set_status(dev_status, TRI_DEV_TIMEOUT);
+    const int is = rc.issued;
+    for (int u = max(0, is - STAGES); u < is; ++u)
+      (void)mbar_wait_bounded(&rc.full[u % STAGES], static_cast<uint32_t>((u / STAGES) & 1));
+  }
+}
 
 template <typename T, int D>
 struct Geo {

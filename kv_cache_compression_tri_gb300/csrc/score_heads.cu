@@ -33,8 +33,9 @@
 namespace tri {
 namespace {
 
-constexpr size_t HEADS_STATS_OFF = (SCORE_SMEM + 15) / 16 * 16;
-constexpr size_t HEADS_SMEM = HEADS_STATS_OFF + SCORE_THREADS * (3 * sizeof(double) + sizeof(int));
+constexpr size_t HEADS_STATS_OFF = SCORE_SMEM;  // 16-byte aligned
+constexpr size_t HEADS_JUMP_OFF = HEADS_STATS_OFF + SCORE_THREADS * (3 * sizeof(double) + sizeof(int));
+constexpr size_t HEADS_SMEM = HEADS_JUMP_OFF + MAX_BANDS / 2 * sizeof(float4);
 
 // Sums a[0..NU) over the TPK lanes of a key group. Each lane ends with RPL =
 // max(1, NU / TPK) consecutive sums, entries idx .. idx + RPL - 1; when NU <
@@ -72,14 +73,17 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
   constexpr int F = G::F, BPT = G::BPT, NP = BPT / 2, TPK = G::TPK, KPW = G::KPW;
   constexpr int ROW_BYTES = G::ROW_BYTES, TILE_ROWS = G::TILE_ROWS, RPW = G::RPW, STEPS = G::STEPS;
   constexpr int GHP = (GH == 3) ? 4 : GH;  // heads padded to a power of two for the reduction
-  constexpr int NU = GHP * STEPS;
+  constexpr int HS = 2;                    // keys per lane between reductions
+  constexpr int NU = GHP * HS;
   constexpr int RPL = (NU >= TPK) ? NU / TPK : 1;
+  static_assert(STEPS % HS == 0, "steps per reduction");
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * TILE_BYTES);
-  volatile int* failed = reinterpret_cast<volatile int*>(full + STAGES);
+  RingCtrl& rc = *reinterpret_cast<RingCtrl*>(smem + RING_BYTES);
   double* spart = reinterpret_cast<double*>(smem + HEADS_STATS_OFF);  // [threads][3]
   int* shead = reinterpret_cast<int*>(spart + 3 * SCORE_THREADS);     // [threads]
+  // per band pair: the tile-to-tile rotation (re0, re1, im0, im1)
+  float4* sjump = reinterpret_cast<float4*>(smem + HEADS_JUMP_OFF);
 
   const int64_t s = blockIdx.x / p.tiles_per_slice;
   const int ct = blockIdx.x % p.tiles_per_slice;
@@ -102,15 +106,14 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
   auto issue = [&](int u) {
     const int rows = min(TILE_ROWS, c1 - c0 - u * TILE_ROWS);
     const uint32_t bytes = static_cast<uint32_t>(rows * ROW_BYTES);
-    uint64_t* bar = &full[u % STAGES];
+    uint64_t* bar = &rc.full[u % STAGES];
     mbar_arrive_expect_tx(bar, bytes);
     bulk_g2s(ring + (u % STAGES) * TILE_BYTES, src + static_cast<int64_t>(u) * TILE_BYTES, bytes, bar);
   };
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int st = 0; st < STAGES; ++st) mbar_init(&full[st], 1);
-    *failed = 0;
-    mbar_init_fence();
+  if (threadIdx.x == 0) ring_init(rc, ntiles);
+  if (threadIdx.x < F / 2) {
+    const int f = 2 * threadIdx.x;
+    sjump[threadIdx.x] = make_float4(p.jump_re[f], p.jump_re[f + 1], p.jump_im[f], p.jump_im[f + 1]);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
   const int64_t seq = s / p.lh_count;
   const int64_t pc = p.p_cur[seq];
   float2 WR[GH][NP], WI[GH][NP], NW[GH][NP];
-  float2 ER[NP], EI[NP], SR[NP], SI[NP], NSI[NP], JR[NP], JI[NP];
+  float2 ER[NP], EI[NP], SR[NP], SI[NP], NSI[NP];
   uint64_t nu[BPT];
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
@@ -164,8 +167,6 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
     SR[q] = f2(p.step_re[f0], p.step_re[f0 + 1]);
     SI[q] = f2(p.step_im[f0], p.step_im[f0 + 1]);
     NSI[q] = f2(-p.step_im[f0], -p.step_im[f0 + 1]);
-    JR[q] = f2(p.jump_re[f0], p.jump_re[f0 + 1]);
-    JI[q] = f2(p.jump_im[f0], p.jump_im[f0 + 1]);
   }
 
   float* out = p.scores_g + (s * p.group + p.head0) * static_cast<int64_t>(p.n_cap);
@@ -176,14 +177,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
   int cnt = 0;
   int lane_head = -1;
 
-  int t = 0;
-  for (; t < ntiles; ++t) {
+  for (int t = 0; t < ntiles; ++t) {
     const int st = t % STAGES;
-    bool ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((t / STAGES) & 1));
-    ok = __all_sync(FULL_MASK, ok);
-    if (!ok) {
-      if (lane == 0) *failed = 1;
-    } else {
+    if (!ring_wait(rc, t, lane)) break;
+    {
       const unsigned char* tile = ring + st * TILE_BYTES;
       const int rbase = warp * RPW + kq;
       int pp[STEPS];
@@ -194,11 +191,14 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
           pp[j] = (r < c1) ? __ldg(pos + r) : 0;
         }
       }
+#pragma unroll
+      for (int h0 = 0; h0 < STEPS; h0 += HS) {
       float acc[NU];
 #pragma unroll
       for (int e = 0; e < NU; ++e) acc[e] = 0.f;
 #pragma unroll
-      for (int j = 0; j < STEPS; ++j) {
+      for (int jj = 0; jj < HS; ++jj) {
+        const int j = h0 + jj;
         const int rt = rbase + j * KPW;
         const bool valid = c0 + t * TILE_ROWS + rt < c1;
         uint4 raw = make_uint4(0u, 0u, 0u, 0u);
@@ -237,16 +237,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
           }
         }
 #pragma unroll
-        for (int g = 0; g < GH; ++g) acc[g * STEPS + j] = a[g].x + a[g].y;
-      }
-      if (!EXPLICIT_POS) {
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-          const float2 er = ER[q], ei = EI[q];
-          const float2 nji = f2(-JI[q].x, -JI[q].y);
-          ER[q] = __ffma2_rn(er, JR[q], __fmul2_rn(ei, nji));
-          EI[q] = __ffma2_rn(er, JI[q], __fmul2_rn(ei, JR[q]));
-        }
+        for (int g = 0; g < GH; ++g) acc[g * HS + jj] = a[g].x + a[g].y;
       }
       int idx;
       float v[RPL];
@@ -254,7 +245,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
 #pragma unroll
       for (int r = 0; r < RPL; ++r) {
         const int e = idx + r;
-        const int g = e / STEPS, j = e % STEPS;
+        const int g = e / HS, j = h0 + e % HS;
         const int row = c0 + t * TILE_ROWS + rbase + j * KPW;
         if (own && g < GH && row < c1) {
           __stcs(out + static_cast<int64_t>(g) * p.n_cap + row, v[r]);
@@ -266,21 +257,24 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
           lane_head = g;
         }
       }
+      }
+      if (!EXPLICIT_POS) {
+        // from this lane's last key of tile t to its first key of tile t + 1
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+          const float4 jq = sjump[c * NP + q];
+          const float2 jr = f2(jq.x, jq.y), ji = f2(jq.z, jq.w), nji = f2(-jq.z, -jq.w);
+          const float2 er = ER[q], ei = EI[q];
+          ER[q] = __ffma2_rn(er, jr, __fmul2_rn(ei, nji));
+          EI[q] = __ffma2_rn(er, ji, __fmul2_rn(ei, jr));
+        }
+      }
     }
-    __syncthreads();  // the whole CTA is done with stage st
-    if (*failed) break;
-    if (threadIdx.x == 0 && t + STAGES < ntiles) {
-      fence_proxy_async_smem();
-      issue(t + STAGES);
-    }
+    ring_release(rc, t, ntiles, lane, issue);
+    if (ring_failed(rc)) break;
   }
-  if (t < ntiles && threadIdx.x == 0) {
-    // A wait timed out: report it and let the copies already in flight land
-    // before the CTA's shared memory is released.
-    set_status(p.dev_status, TRI_DEV_TIMEOUT);
-    for (int u = t; u < min(ntiles, t + STAGES); ++u)
-      (void)mbar_wait_bounded(&full[u % STAGES], static_cast<uint32_t>((u / STAGES) & 1));
-  }
+  __syncthreads();
+  ring_drain(rc, p.dev_status);
 
   // ---- statistics partials of this CTA, per head, in fp64 -------------------
   {
