@@ -26,6 +26,10 @@ Parity status of each function (what pins it, all in ``tests/test_oracle_*``):
                         uniformity statistics.
   rand_select        -- inclusion frequency, the survival-by-age law of
                         Random Attention, slot coverage across heads.
+  rope_rows          -- the rotation itself: a round trip is the identity,
+                        one band is the complex product by e^{i w p}.
+  score_post_rope    -- inverse RoPE, then score_series; equals the
+                        pre-RoPE score of the un-rotated keys.
   score_heads        -- per-query-head scores: score_series once per head;
                         identical heads reduce to the pooled score.
   zscore_max         -- a hand-worked two-head example in closed form,
@@ -90,6 +94,8 @@ def _load():
             lib.orc_rand_u32.restype = u32
             lib.orc_rand_select.argtypes = [u64, u32, i64, i64, i64, i64, i64, i64, i64, vp]
             lib.orc_rand_select.restype = i32
+            lib.orc_rope_rows.argtypes = [vp, vp, i64, i64, i32, dbl, i32, vp]
+            lib.orc_rope_rows.restype = None
             lib.orc_zscore_max.argtypes = [vp, i64, i64, vp, vp, vp]
             lib.orc_zscore_max.restype = None
             _lib = lib
@@ -242,3 +248,25 @@ def zscore_max(scores_g):
     mean, std, final = np.zeros(G), np.zeros(G), np.zeros(n)
     _load().orc_zscore_max(_ptr(s), G, n, _ptr(mean), _ptr(std), _ptr(final))
     return mean, std, final
+
+
+def rope_rows(x, pos, theta: float, style: int = ROPE_INTERLEAVED, inverse: bool = False) -> np.ndarray:
+    """RoPE of every row: row i rotated by omega_f * pos_i, or by -omega_f *
+    pos_i when inverse (TriAttention summary page, "RoPE in complex form";
+    the blog's invert_rope)."""
+    x = _f64(x)
+    n, d = x.shape
+    p = _i64(pos)
+    assert p.shape == (n,)
+    out = np.zeros_like(x)
+    _load().orc_rope_rows(_ptr(x), _ptr(p), n, d, style, float(theta), -1 if inverse else 1, _ptr(out))
+    return out
+
+
+def score_post_rope(k_post, pos, center, mean_norm, mrl, offsets, p_cur: int, theta: float,
+                    style: int = ROPE_INTERLEAVED, norm_mode: int = NORM_WEIGHTED) -> np.ndarray:
+    """Score of post-RoPE cached keys (the layout engines keep): undo RoPE with
+    each row's position, then the pre-RoPE series (the blog's scoring step)."""
+    k = rope_rows(k_post, pos, theta, style=style, inverse=True)
+    return score_series(k, center, mean_norm, mrl, offsets, p_cur, theta, pos=pos, style=style,
+                        norm_mode=norm_mode)

@@ -189,6 +189,19 @@ void orc_score_series(const double* k, const int64_t* pos, int64_t n, int64_t d,
 }
 
 // ---------------------------------------------------------------------------
+// RoPE of whole rows ([TA] "RoPE in complex form"; [TB] "scoring": an engine
+// stores post-RoPE keys and invert_rope undoes the rotation before scoring):
+// row i of x is rotated by +omega_f pos_i (sign = +1, what an engine stores)
+// or by -omega_f pos_i (sign = -1, the inverse). x, out: [n][d]; pos [n].
+// ---------------------------------------------------------------------------
+void orc_rope_rows(const double* x, const int64_t* pos, int64_t n, int64_t d, int style, double theta,
+                   int sign, double* out) {
+  for (int64_t i = 0; i < n; ++i)
+    rope_rotate(x + i * d, d, style, theta, static_cast<double>(sign) * static_cast<double>(pos[i]),
+                out + i * d);
+}
+
+// ---------------------------------------------------------------------------
 // Score by brute force, one slice (tiny inputs only). The centre, written as a
 // real d-vector, stands in for a future query ([TA] "Why the Q center, not
 // actual queries"): rotate it to p_cur + delta and the key to p_k with

@@ -193,3 +193,43 @@ def test_norm_identity_on_calibrated_stats():
     rhs = m - np.hypot(c[..., 0], c[..., 1])
     assert np.allclose(lhs, rhs, rtol=0, atol=1e-13)
     assert np.all(R <= 1 + 1e-15) and np.all(R >= 0)
+
+
+# ---- post-RoPE layout: RoPE of rows and its inverse -------------------------
+def test_rope_rows_round_trip_and_single_band():
+    rng = np.random.default_rng(21)
+    for style in (0, 1):
+        x = rng.normal(size=(50, 64))
+        pos = rng.integers(0, 100000, size=50)
+        y = orc.rope_rows(x, pos, 1e4, style=style)
+        assert np.allclose(orc.rope_rows(y, pos, 1e4, style=style, inverse=True), x, atol=1e-9)
+        # rotation keeps every band's magnitude
+        F = 32
+        def bands(v):
+            return (v[:, 0::2] + 1j * v[:, 1::2]) if style == 0 else (v[:, :F] + 1j * v[:, F:])
+        assert np.allclose(np.abs(bands(y)), np.abs(bands(x)), atol=1e-9)
+    # d = 4, theta = 100: omega = (1, 0.1); band f multiplied by e^{i omega_f p}
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    y = orc.rope_rows(x, [7], 100.0)
+    z0 = (1 + 2j) * np.exp(1j * 7.0)
+    z1 = (3 + 4j) * np.exp(1j * 0.7)
+    assert np.allclose(y[0], [z0.real, z0.imag, z1.real, z1.imag], atol=1e-12)
+
+
+def test_post_rope_score_equals_pre_rope_score():
+    rng = np.random.default_rng(22)
+    n, d, F = 200, 64, 32
+    k = rng.normal(size=(n, d)) + 1.5
+    pos = np.sort(rng.choice(5000, size=n, replace=False))
+    c = rng.normal(size=(F, 2)) * 2
+    m = np.hypot(c[:, 0], c[:, 1]) * 1.3
+    R = np.hypot(c[:, 0], c[:, 1]) / m
+    offs = [1, 4, 16, 64]
+    for style in (0, 1):
+        pre = orc.score_series(k, c, m, R, offs, 5003, 1e4, pos=pos, style=style)
+        kp = orc.rope_rows(k, pos, 1e4, style=style)
+        post = orc.score_post_rope(kp, pos, c, m, R, offs, 5003, 1e4, style=style)
+        assert np.allclose(post, pre, rtol=0, atol=1e-9 * np.abs(pre).max())
+        # and the brute-force dot product of the rotated centre with the stored key
+        bf = orc.score_bruteforce(k, c, m, R, offs, 5003, 1e4, pos=pos, style=style)
+        assert np.allclose(post, bf, rtol=0, atol=1e-9 * np.abs(pre).max())
