@@ -289,6 +289,7 @@ def workload_config(w, path: str = "separate") -> dict:
         "head_dim": w.head_dim, "n_cap": w.n_cap, "n_valid": w.n_valid, "budget": w.budget,
         "n_prompt": w.n_prompt, "n_recent": w.n_recent, "offsets": len(w.offsets),
         "rope_theta": w.theta, "storage": "bf16" if w.elem_bytes == 2 else "f32",
+        "keys": "post-RoPE" if w.key_layout == "post" else "pre-RoPE",
         "path": ("rand_evict + tri_compact_kv" if w.random else
                  ("tri_compress (score, select, compact in one call)" if path == "compress" else
                   ("tri_score_heads + tri_select_topk_zmax + tri_compact_kv (GQA z-score + max, group %d)"
@@ -335,7 +336,7 @@ def run_gpu(args, w):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     n_valid = torch.full((S,), n, dtype=torch.int32, device=dev)
     pos_out = torch.empty(S, w.n_cap, dtype=torch.int32, device=dev)
-    kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status)
+    kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status, post_rope=(w.key_layout == "post"))
     fused = (args.path == "compress") and not w.random
     scores = None if (fused or gqa) else torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
     if gqa:
@@ -577,6 +578,54 @@ def measure_other(args, tri, synth, dev):
     del inp, kh, vh, kv, keep, scores_g, stats, hws
     torch.cuda.empty_cache()
 
+    # ---- the stack with post-RoPE keys (the engine layout) ------------------
+    w = synth.WORKLOADS["qwen3_8b_stack_post_rope"]
+    S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    inp = synth.make_inputs(w, dev)
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    torch.cuda.empty_cache()
+    kh, vh = inp.k[:, :, :, :B].clone(), inp.v[:, :, :, :B].clone()
+    nv = torch.full((S,), n, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = tri.KVCache(inp.k, inp.v, nv, None, torch.empty(S, w.n_cap, dtype=torch.int32, device=dev), st,
+                     post_rope=True)
+    scores = torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+    kms = []
+
+    def post_event():
+        e = [ev() for _ in range(4)]
+        e[0].record()
+        tri.score(kv, c, w.theta, w.offsets, inp.p_cur, scores, n_prompt=P, n_recent=W)
+        e[1].record()
+        tri.select_topk(scores, kv, P, W, B, keep)
+        e[2].record()
+        tri.compact_kv(kv, keep, B)
+        e[3].record()
+        kms.append(e)
+
+    def restore_q():
+        inp.k[:, :, :, :B].copy_(kh)
+        inp.v[:, :, :, :B].copy_(vh)
+        nv.fill_(n)
+
+    ms = timed(post_event, restore_q)
+    kt = [[x[0].elapsed_time(x[1]), x[1].elapsed_time(x[2]), x[2].elapsed_time(x[3])] for x in kms[args.warmup:]]
+    k_ms = [sum(x[j] for x in kt) / len(kt) for j in range(3)]
+    moved = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
+    score_by = S * (n - P - W) * w.head_dim * w.elem_bytes
+    by = score_by + moved * (4 * w.head_dim * w.elem_bytes + 8)
+    assert int(st.item()) == 0
+    out[w.name] = {
+        "value": S * n / (ms / 1e3), "unit": UNIT, "ms_per_event": ms, "gbs": by / ms / 1e6,
+        "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
+        "algorithmic_bytes": by,
+        "kernel_ms": {"score": round(k_ms[0], 4), "select": round(k_ms[1], 4), "compact": round(k_ms[2], 4)},
+        "score_gbs": score_by / k_ms[0] / 1e6, "score_frac_of_measured_peak": score_by / k_ms[0] / 1e6 / peak}
+    del inp, kh, vh, kv, keep, scores
+    torch.cuda.empty_cache()
+
     # ---- large-batch periodic -----------------------------------------------
     w = synth.WORKLOADS["periodic_large_batch"]
     S, n, P, W, B, R, d, e = (w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget, w.round_rows,
@@ -700,7 +749,7 @@ def run_e2e(args, w, tri, synth, inp, centers, dev, stream):
     n_valid = torch.full((Se,), n, dtype=torch.int32, device=dev)
     pos_out = torch.empty(Se, w.n_cap, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    kv = tri.KVCache(dk, dv, n_valid, None, pos_out, status)
+    kv = tri.KVCache(dk, dv, n_valid, None, pos_out, status, post_rope=(w.key_layout == "post"))
     scores = None
     keep = torch.empty(Se, B, dtype=torch.int32, device=dev)
     p_cur = inp.p_cur[:n_seq]

@@ -76,12 +76,21 @@ typedef enum { TRI_ROPE_INTERLEAVED = 0, TRI_ROPE_HALF = 1 } tri_rope_style;
  * S_norm^(0) = sum_f E|q_f| |k_f| ([TA] "The Norm-Based Term"). */
 typedef enum { TRI_NORM_WEIGHTED = 0, TRI_NORM_UNWEIGHTED = 1 } tri_norm_mode;
 
+/* What the cached K rows hold. Pre-RoPE keys k_i (the form [TA] scores) with
+ * their positions in `pos`; or post-RoPE keys k~_i = RoPE(k_i, p_i), band f
+ * multiplied by e^{i w_f p_i} in the same pairing style -- what engines store
+ * ([TB] "scoring": vLLM keeps post-RoPE K and inverts RoPE before scoring;
+ * [RA] Appendix F). For post-RoPE keys the score needs no positions: with
+ * k_f = e^{-i w_f p_i} k~_f it is Re sum_f c_f G_f e^{i w_f p_cur} conj(k~_f)
+ * + sum_f wgt_f E|q_f| |k~_f|, the same value. */
+typedef enum { TRI_KEYS_PRE_ROPE = 0, TRI_KEYS_POST_ROPE = 1 } tri_key_layout;
+
 /* The cache. K and V rows are head_dim elements, contiguous; slice s starts
  * at element s * slice_stride of k (and of v); row i of the slice at element
  * s * slice_stride + i * head_dim. k and v: device, 16-byte aligned,
  * slice_stride * element size a multiple of 16 bytes. */
 typedef struct {
-  void* k;               /* [n_slices][n_cap][head_dim] pre-RoPE keys            */
+  void* k;               /* [n_slices][n_cap][head_dim] keys (see key_layout)    */
   void* v;               /* [n_slices][n_cap][head_dim] values                   */
   int32_t* pos;          /* device [n_slices][n_cap] token positions, or NULL:
                             NULL means position = slot index (a fresh cache)    */
@@ -95,6 +104,7 @@ typedef struct {
   int32_t head_dim;      /* 64 or 128                                            */
   tri_dtype dtype;       /* element type of k and v                              */
   int32_t* dev_status;   /* device int32 status word (TRI_DEV_*), or NULL        */
+  tri_key_layout key_layout; /* pre- or post-RoPE keys (0 = pre-RoPE)            */
 } tri_kv;
 
 /* Per-(layer, KV head) query statistics, [TA] "Offline Calibration
@@ -107,7 +117,7 @@ typedef struct {
 
 /* ------------------------------------------------------------------------ */
 const char* tri_status_string(tri_status s); /* static text, never NULL */
-int32_t tri_abi_version(void);               /* 1 */
+int32_t tri_abi_version(void);               /* 2 */
 /* Kernels this library has launched in this process (all devices, all
  * threads); used to count launches inside a timed region. */
 uint64_t tri_launch_count(void);

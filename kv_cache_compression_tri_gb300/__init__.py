@@ -21,7 +21,8 @@ from ._build import LIB as _LIB_PATH
 __all__ = [
     "TriError", "KVCache", "Centers", "lib_path", "load_library", "calibrate_centers",
     "calibrate_workspace_bytes", "score", "select_topk", "compact_kv", "rand_evict",
-    "compress", "compress_workspace_bytes",
+    "compress", "compress_workspace_bytes", "score_heads", "score_heads_workspace_bytes",
+    "select_topk_zmax",
     "launch_count", "ROPE_INTERLEAVED", "ROPE_HALF", "NORM_WEIGHTED", "NORM_UNWEIGHTED",
     "DEV_OK", "DEV_NVALID_OVER_CAP", "DEV_NAN_SCORE", "DEV_BAD_KEEP",
 ]
@@ -47,7 +48,7 @@ class _TriKV(ctypes.Structure):
         ("slice_stride", ctypes.c_int64), ("n_seq", ctypes.c_int32),
         ("n_layers", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
         ("n_cap", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int),
-        ("dev_status", ctypes.c_void_p),
+        ("dev_status", ctypes.c_void_p), ("key_layout", ctypes.c_int),
     ]
 
 
@@ -150,13 +151,15 @@ class Centers:
 class KVCache:
     """A batch of caches: k, v [n_seq, n_layers, n_kv_heads, n_cap, head_dim]
     (bf16 or fp32, device); n_valid [S] int32; pos / pos_out [S, n_cap] int32
-    (pos may be None: position = slot index); dev_status [1] int32."""
+    (pos may be None: position = slot index); dev_status [1] int32.
+    post_rope: k holds RoPE-rotated keys (the score then ignores pos)."""
     k: torch.Tensor
     v: torch.Tensor
     n_valid: torch.Tensor
     pos: torch.Tensor | None
     pos_out: torch.Tensor | None
     dev_status: torch.Tensor | None = None
+    post_rope: bool = False
 
     @property
     def shape(self):
@@ -182,7 +185,7 @@ class KVCache:
                 assert t.dtype == torch.int32 and t.is_contiguous() and t.numel() == n_seq * L * H * n_cap
         return _TriKV(self.k.data_ptr(), self.v.data_ptr(), _ptr(self.pos), _ptr(self.pos_out),
                       self.n_valid.data_ptr(), stride, n_seq, L, H, n_cap, d, _DTYPES[self.k.dtype],
-                      _ptr(self.dev_status))
+                      _ptr(self.dev_status), 1 if self.post_rope else 0)
 
 
 def calibrate_workspace_bytes(n_layers: int, n_q_heads: int, group: int, head_dim: int,

@@ -62,10 +62,11 @@ __device__ __forceinline__ float reduce_scatter(float (&a)[NU], int lane, int& i
   return r;
 }
 
-template <typename T, int D, int STYLE, bool EXPLICIT_POS>
+template <typename T, int D, int STYLE, int PM>
 __global__ void __launch_bounds__(SCORE_THREADS, 3)
     score_kernel(const __grid_constant__ ScoreParams p) {
   using G = Geo<T, D>;
+  constexpr bool EXPLICIT_POS = PM == POS_EXPLICIT, POST = PM == POS_POST_ROPE;
   constexpr int F = G::F, BPT = G::BPT, NP = BPT / 2, TPK = G::TPK, KPW = G::KPW;
   constexpr int ROW_BYTES = G::ROW_BYTES, TILE_ROWS = G::TILE_ROWS, RPW = G::RPW, STEPS = G::STEPS;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -124,7 +125,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
       wi[h] = w.y;
       nu[2 * q + h] = p.nu[f];
       if (!EXPLICIT_POS) {
-        const float2 d = cmul(w, turns_rotation_accurate(pc - (c0 + warp * RPW + kq), p.nu[f]));
+        // post-RoPE: the constant e^{i w p_cur}; slot positions: the first key's rotation
+        const int64_t delta = POST ? pc : pc - (c0 + warp * RPW + kq);
+        const float2 d = cmul(w, turns_rotation_accurate(delta, p.nu[f]));
         dr[h] = d.x;
         di[h] = d.y;
       }
@@ -184,6 +187,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
             const float2 C = f2(r0.x, r1.x), S = f2(r0.y, r1.y);
             dr = __ffma2_rn(WR[q], C, __fmul2_rn(WI[q], f2(-S.x, -S.y)));
             di = __ffma2_rn(WR[q], S, __fmul2_rn(WI[q], C));
+          } else if (POST) {
+            dr = DR[q];
+            di = DI[q];
           } else {
             dr = DR[q];
             di = DI[q];
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
         }
         acc[j] = a2.x + a2.y;
       }
-      if (!EXPLICIT_POS) {
+      if (PM == POS_SLOT) {
         // from this lane's last key of tile t to its first key of tile t + 1
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -227,9 +233,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   ring_drain(rc, p.dev_status);
 }
 
-template <typename T, int D, int STYLE, bool EXPLICIT_POS>
+template <typename T, int D, int STYLE, int PM>
 cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
-  auto kern = score_kernel<T, D, STYLE, EXPLICIT_POS>;
+  auto kern = score_kernel<T, D, STYLE, PM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SCORE_SMEM));
   if (e != cudaSuccess) return e;
@@ -239,14 +245,17 @@ cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <typename T, int D, int STYLE>
+cudaError_t launch_pm(const ScoreParams& p, int pm, int n_slices, cudaStream_t st) {
+  if (pm == POS_POST_ROPE) return launch_one<T, D, STYLE, POS_POST_ROPE>(p, n_slices, st);
+  if (pm == POS_EXPLICIT) return launch_one<T, D, STYLE, POS_EXPLICIT>(p, n_slices, st);
+  return launch_one<T, D, STYLE, POS_SLOT>(p, n_slices, st);
+}
+
 template <typename T, int D>
-cudaError_t launch_style(const ScoreParams& p, tri_rope_style style, bool explicit_pos, int n_slices,
-                         cudaStream_t st) {
-  if (style == TRI_ROPE_INTERLEAVED)
-    return explicit_pos ? launch_one<T, D, TRI_ROPE_INTERLEAVED, true>(p, n_slices, st)
-                        : launch_one<T, D, TRI_ROPE_INTERLEAVED, false>(p, n_slices, st);
-  return explicit_pos ? launch_one<T, D, TRI_ROPE_HALF, true>(p, n_slices, st)
-                      : launch_one<T, D, TRI_ROPE_HALF, false>(p, n_slices, st);
+cudaError_t launch_style(const ScoreParams& p, tri_rope_style style, int pm, int n_slices, cudaStream_t st) {
+  if (style == TRI_ROPE_INTERLEAVED) return launch_pm<T, D, TRI_ROPE_INTERLEAVED>(p, pm, n_slices, st);
+  return launch_pm<T, D, TRI_ROPE_HALF>(p, pm, n_slices, st);
 }
 
 template <typename T, int D>
@@ -263,13 +272,13 @@ ScoreGeometry score_geometry(tri_dtype dt, int head_dim) {
 }
 
 cudaError_t launch_score(const ScoreParams& p, tri_dtype dt, int head_dim, tri_rope_style style,
-                         bool explicit_pos, int n_slices, cudaStream_t st) {
+                         int pos_mode, int n_slices, cudaStream_t st) {
   if (dt == TRI_BF16) {
-    if (head_dim == 128) return launch_style<uint16_t, 128>(p, style, explicit_pos, n_slices, st);
-    return launch_style<uint16_t, 64>(p, style, explicit_pos, n_slices, st);
+    if (head_dim == 128) return launch_style<uint16_t, 128>(p, style, pos_mode, n_slices, st);
+    return launch_style<uint16_t, 64>(p, style, pos_mode, n_slices, st);
   }
-  if (head_dim == 128) return launch_style<float, 128>(p, style, explicit_pos, n_slices, st);
-  return launch_style<float, 64>(p, style, explicit_pos, n_slices, st);
+  if (head_dim == 128) return launch_style<float, 128>(p, style, pos_mode, n_slices, st);
+  return launch_style<float, 64>(p, style, pos_mode, n_slices, st);
 }
 
 }  // namespace tri

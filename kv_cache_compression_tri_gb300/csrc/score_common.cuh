@@ -105,6 +105,13 @@ struct Geo {
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// Where the rotation e^{i w_f (p_cur - p)} of a key comes from.
+enum PosMode : int {
+  POS_SLOT = 0,       // pre-RoPE keys at position = slot: one complex multiply per key advances it
+  POS_EXPLICIT = 1,   // pre-RoPE keys with a position array: evaluated per key from the fixed-point phase
+  POS_POST_ROPE = 2,  // post-RoPE keys carry e^{-i w_f p} already: only the constant e^{i w_f p_cur} remains
+};
+
 // 16 bytes of one key row for lane group c, from shared memory.
 template <typename T, int D, int STYLE>
 __device__ __forceinline__ uint4 lds_chunk(const unsigned char* row, int c) {

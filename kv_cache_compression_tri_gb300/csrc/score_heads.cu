@@ -66,10 +66,11 @@ __device__ __forceinline__ void reduce_heads(float (&a)[NU], int lane, int& idx,
   }
 }
 
-template <typename T, int D, int STYLE, bool EXPLICIT_POS, int GH>
+template <typename T, int D, int STYLE, int PM, int GH>
 __global__ void __launch_bounds__(SCORE_THREADS, 2)
     score_heads_kernel(const __grid_constant__ ScoreParams p) {
   using G = Geo<T, D>;
+  constexpr bool EXPLICIT_POS = PM == POS_EXPLICIT, POST = PM == POS_POST_ROPE;
   constexpr int F = G::F, BPT = G::BPT, NP = BPT / 2, TPK = G::TPK, KPW = G::KPW;
   constexpr int ROW_BYTES = G::ROW_BYTES, TILE_ROWS = G::TILE_ROWS, RPW = G::RPW, STEPS = G::STEPS;
   constexpr int GHP = (GH == 3) ? 4 : GH;  // heads padded to a power of two for the reduction
@@ -137,7 +138,9 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
       const int f = c * BPT + 2 * q + h;
       nu[2 * q + h] = p.nu[f];
       if (!EXPLICIT_POS) {
-        const float2 e = turns_rotation_accurate(pc - (c0 + warp * RPW + kq), p.nu[f]);
+        // post-RoPE: the constant e^{i w p_cur}; slot positions: the first key's rotation
+        const int64_t delta = POST ? pc : pc - (c0 + warp * RPW + kq);
+        const float2 e = turns_rotation_accurate(delta, p.nu[f]);
         er[h] = e.x;
         ei[h] = e.y;
       }
@@ -153,7 +156,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
         const float m = p.mean_norm[row];
         const float R = p.mrl[row];
         nw[h] = (p.norm_mode == TRI_NORM_UNWEIGHTED) ? m : (1.0f - R) * m;
-        const float2 w = cmul(cf, make_float2(p.g_re[f], p.g_im[f]));
+        float2 w = cmul(cf, make_float2(p.g_re[f], p.g_im[f]));
+        if (POST) w = cmul(w, make_float2(er[h], ei[h]));  // fold the constant rotation in
         wr[h] = w.x;
         wi[h] = w.y;
       }
@@ -212,6 +216,18 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
         for (int q = 0; q < NP; ++q) {
           const float2 RE = f2(re[2 * q], re[2 * q + 1]);
           const float2 IM = f2(im[2 * q], im[2 * q + 1]);
+          const float2 sq = __ffma2_rn(IM, IM, __fmul2_rn(RE, RE));
+          const float2 mag = f2(sqrt_approx(sq.x), sqrt_approx(sq.y));
+          if (POST) {
+            // Re(W e^{i w p_cur} conj(k~)) = Re(W') Re k~ + Im(W') Im k~
+#pragma unroll
+            for (int g = 0; g < GH; ++g) {
+              a[g] = __ffma2_rn(WR[g][q], RE, a[g]);
+              a[g] = __ffma2_rn(WI[g][q], IM, a[g]);
+              a[g] = __ffma2_rn(NW[g][q], mag, a[g]);
+            }
+            continue;
+          }
           float2 er, ei;
           if (EXPLICIT_POS) {
             const float2 r0 = turns_rotation_fast(pc - pp[j], nu[2 * q]);
@@ -227,8 +243,6 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
           // z = e conj(k): Re z = er kr + ei ki; -Im z = er ki - ei kr
           const float2 zr = __ffma2_rn(er, RE, __fmul2_rn(ei, IM));
           const float2 zn = __ffma2_rn(er, IM, __fmul2_rn(ei, f2(-RE.x, -RE.y)));
-          const float2 sq = __ffma2_rn(IM, IM, __fmul2_rn(RE, RE));
-          const float2 mag = f2(sqrt_approx(sq.x), sqrt_approx(sq.y));
 #pragma unroll
           for (int g = 0; g < GH; ++g) {
             a[g] = __ffma2_rn(WR[g][q], zr, a[g]);
@@ -258,7 +272,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
         }
       }
       }
-      if (!EXPLICIT_POS) {
+      if (PM == POS_SLOT) {
         // from this lane's last key of tile t to its first key of tile t + 1
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -344,9 +358,9 @@ __global__ void zmax_scores_kernel(const float* __restrict__ scores_g, const flo
   out[s * static_cast<int64_t>(n_cap) + i] = best;
 }
 
-template <typename T, int D, int STYLE, bool EXPLICIT_POS, int GH>
+template <typename T, int D, int STYLE, int PM, int GH>
 cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
-  auto kern = score_heads_kernel<T, D, STYLE, EXPLICIT_POS, GH>;
+  auto kern = score_heads_kernel<T, D, STYLE, PM, GH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(HEADS_SMEM));
   if (e != cudaSuccess) return e;
@@ -356,37 +370,41 @@ cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <typename T, int D, int STYLE, bool EXPLICIT_POS>
+template <typename T, int D, int STYLE, int PM>
 cudaError_t launch_heads(const ScoreParams& p, int n_heads, int n_slices, cudaStream_t st) {
   switch (n_heads) {
-    case 1: return launch_one<T, D, STYLE, EXPLICIT_POS, 1>(p, n_slices, st);
-    case 2: return launch_one<T, D, STYLE, EXPLICIT_POS, 2>(p, n_slices, st);
-    case 3: return launch_one<T, D, STYLE, EXPLICIT_POS, 3>(p, n_slices, st);
-    case 4: return launch_one<T, D, STYLE, EXPLICIT_POS, 4>(p, n_slices, st);
+    case 1: return launch_one<T, D, STYLE, PM, 1>(p, n_slices, st);
+    case 2: return launch_one<T, D, STYLE, PM, 2>(p, n_slices, st);
+    case 3: return launch_one<T, D, STYLE, PM, 3>(p, n_slices, st);
+    case 4: return launch_one<T, D, STYLE, PM, 4>(p, n_slices, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
+template <typename T, int D, int STYLE>
+cudaError_t launch_pm(const ScoreParams& p, int n_heads, int pm, int n_slices, cudaStream_t st) {
+  if (pm == POS_POST_ROPE) return launch_heads<T, D, STYLE, POS_POST_ROPE>(p, n_heads, n_slices, st);
+  if (pm == POS_EXPLICIT) return launch_heads<T, D, STYLE, POS_EXPLICIT>(p, n_heads, n_slices, st);
+  return launch_heads<T, D, STYLE, POS_SLOT>(p, n_heads, n_slices, st);
+}
+
 template <typename T, int D>
-cudaError_t launch_style(const ScoreParams& p, int n_heads, tri_rope_style style, bool explicit_pos,
-                         int n_slices, cudaStream_t st) {
-  if (style == TRI_ROPE_INTERLEAVED)
-    return explicit_pos ? launch_heads<T, D, TRI_ROPE_INTERLEAVED, true>(p, n_heads, n_slices, st)
-                        : launch_heads<T, D, TRI_ROPE_INTERLEAVED, false>(p, n_heads, n_slices, st);
-  return explicit_pos ? launch_heads<T, D, TRI_ROPE_HALF, true>(p, n_heads, n_slices, st)
-                      : launch_heads<T, D, TRI_ROPE_HALF, false>(p, n_heads, n_slices, st);
+cudaError_t launch_style(const ScoreParams& p, int n_heads, tri_rope_style style, int pm, int n_slices,
+                         cudaStream_t st) {
+  if (style == TRI_ROPE_INTERLEAVED) return launch_pm<T, D, TRI_ROPE_INTERLEAVED>(p, n_heads, pm, n_slices, st);
+  return launch_pm<T, D, TRI_ROPE_HALF>(p, n_heads, pm, n_slices, st);
 }
 
 }  // namespace
 
 cudaError_t launch_score_heads(const ScoreParams& p, int n_heads, tri_dtype dt, int head_dim,
-                               tri_rope_style style, bool explicit_pos, int n_slices, cudaStream_t st) {
+                               tri_rope_style style, int pos_mode, int n_slices, cudaStream_t st) {
   if (dt == TRI_BF16) {
-    if (head_dim == 128) return launch_style<uint16_t, 128>(p, n_heads, style, explicit_pos, n_slices, st);
-    return launch_style<uint16_t, 64>(p, n_heads, style, explicit_pos, n_slices, st);
+    if (head_dim == 128) return launch_style<uint16_t, 128>(p, n_heads, style, pos_mode, n_slices, st);
+    return launch_style<uint16_t, 64>(p, n_heads, style, pos_mode, n_slices, st);
   }
-  if (head_dim == 128) return launch_style<float, 128>(p, n_heads, style, explicit_pos, n_slices, st);
-  return launch_style<float, 64>(p, n_heads, style, explicit_pos, n_slices, st);
+  if (head_dim == 128) return launch_style<float, 128>(p, n_heads, style, pos_mode, n_slices, st);
+  return launch_style<float, 64>(p, n_heads, style, pos_mode, n_slices, st);
 }
 
 cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slices, int tiles_per_slice,

@@ -41,7 +41,14 @@ tri_status check_kv(const tri_kv* kv, bool need_v) {
   if (kv->pos && !aligned(kv->pos, 4)) return TRI_ERR_INVALID_ARG;
   if (kv->pos_out && !aligned(kv->pos_out, 4)) return TRI_ERR_INVALID_ARG;
   if (kv->dev_status && !aligned(kv->dev_status, 4)) return TRI_ERR_INVALID_ARG;
+  if (kv->key_layout != TRI_KEYS_PRE_ROPE && kv->key_layout != TRI_KEYS_POST_ROPE) return TRI_ERR_INVALID_ARG;
   return TRI_OK;
+}
+
+// Where the score kernels take each key's rotation from (see launch_score).
+int pos_mode(const tri_kv* kv) {
+  if (kv->key_layout == TRI_KEYS_POST_ROPE) return 2;
+  return kv->pos ? 1 : 0;
 }
 
 int64_t slices_of(const tri_kv* kv) {
@@ -79,7 +86,7 @@ const char* tri_status_string(tri_status s) {
   return "unknown status";
 }
 
-int32_t tri_abi_version(void) { return 1; }
+int32_t tri_abi_version(void) { return 2; }
 
 uint64_t tri_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -238,7 +245,7 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
   const tri_status st = prepare_score(kv, c, rope_theta, style, norm_mode, offsets, n_offsets, p_cur,
                                       n_prompt, n_recent, scores, false, p);
   if (st != TRI_OK) return st;
-  const cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, kv->pos != nullptr,
+  const cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, pos_mode(kv),
                                      static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
@@ -264,7 +271,7 @@ tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_thet
                      scores, true, p);
   if (st != TRI_OK) return st;
   const int n_slices = static_cast<int>(slices_of(kv));
-  cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, kv->pos != nullptr, n_slices, stream);
+  cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, pos_mode(kv), n_slices, stream);
   if (e != cudaSuccess) return TRI_ERR_CUDA;
   e = launch_select(select_params(scores, kv, n_prompt, n_recent, budget, keep_idx), n_slices, stream);
   if (e != cudaSuccess) return TRI_ERR_CUDA;
@@ -340,7 +347,7 @@ tri_status tri_score_heads(const tri_kv* kv, const tri_centers* centers, int32_t
   for (int h0 = 0; h0 < group; h0 += MAX_HEADS_PER_LAUNCH) {
     p.head0 = h0;
     const int nh = group - h0 < MAX_HEADS_PER_LAUNCH ? group - h0 : MAX_HEADS_PER_LAUNCH;
-    const cudaError_t e = launch_score_heads(p, nh, kv->dtype, kv->head_dim, style, kv->pos != nullptr,
+    const cudaError_t e = launch_score_heads(p, nh, kv->dtype, kv->head_dim, style, pos_mode(kv),
                                              n_slices, stream);
     if (e != cudaSuccess) return TRI_ERR_CUDA;
   }

@@ -254,8 +254,10 @@ struct CalibParams {
 };
 
 // Launchers (return cudaSuccess or the launch error).
+// pos_mode: 0 pre-RoPE keys at their slot index, 1 pre-RoPE keys with a
+// position array, 2 post-RoPE keys (positions unused).
 cudaError_t launch_score(const ScoreParams& p, tri_dtype dt, int head_dim, tri_rope_style style,
-                         bool explicit_pos, int n_slices, cudaStream_t st);
+                         int pos_mode, int n_slices, cudaStream_t st);
 // Score kernel geometry, shared by the launcher and the host constant table:
 // positions between consecutive keys of one lane inside a tile, and the
 // positions skipped from a lane's last key of a tile to its first of the next.
@@ -272,7 +274,7 @@ cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st);
 constexpr int MAX_HEADS_PER_LAUNCH = 4;
 constexpr int MAX_GROUP = 8;
 cudaError_t launch_score_heads(const ScoreParams& p, int n_heads, tri_dtype dt, int head_dim,
-                               tri_rope_style style, bool explicit_pos, int n_slices, cudaStream_t st);
+                               tri_rope_style style, int pos_mode, int n_slices, cudaStream_t st);
 cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slices, int tiles_per_slice,
                                int group, cudaStream_t st);
 cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid,

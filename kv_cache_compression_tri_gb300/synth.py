@@ -16,6 +16,11 @@ stated, in this order):
      in fp32 and rounded once to the cache dtype.
 Rows appended by the periodic workload in round r come from a generator
 seeded with (seed * 1_000_003 + 1 + r) and follow step 4.
+
+Workloads with key_layout "post" store what an engine stores: each key row
+rotated by the model's RoPE at its slot position (rope_rows below; RoPE is
+the model's position encoding, not part of the compression method), drawn
+in fp32 and rounded once to the cache dtype.
 """
 from __future__ import annotations
 
@@ -50,6 +55,7 @@ class Workload:
     rounds: int = 0  # periodic rounds after the first compression
     round_rows: int = 0
     seed: int = 0
+    key_layout: str = "pre"  # "post": keys stored RoPE-rotated at their slot positions
     description: str = ""
 
     @property
@@ -112,6 +118,12 @@ WORKLOADS["qwen3_8b_stack_1seq"] = scaled(WORKLOADS["qwen3_8b_stack"], name="qwe
                                           description="one sequence of the Qwen3-8B-shaped stack")
 WORKLOADS["random_stack_1seq"] = scaled(WORKLOADS["random_stack"], name="random_stack_1seq", n_seq=1,
                                         description="one sequence of the Random Attention stack")
+WORKLOADS["qwen3_8b_stack_post_rope"] = scaled(
+    WORKLOADS["qwen3_8b_stack"], name="qwen3_8b_stack_post_rope", key_layout="post",
+    description="the Qwen3-8B-shaped stack with keys stored post-RoPE, as engines keep them")
+WORKLOADS["qwen3_8b_stack_post_rope_1seq"] = scaled(
+    WORKLOADS["qwen3_8b_stack_post_rope"], name="qwen3_8b_stack_post_rope_1seq", n_seq=1,
+    description="one sequence of the post-RoPE stack")
 WORKLOADS["periodic_1seq"] = scaled(WORKLOADS["periodic_large_batch"], name="periodic_1seq", n_seq=1,
                                     description="one sequence of the large-batch periodic workload")
 
@@ -119,6 +131,30 @@ WORKLOADS["periodic_1seq"] = scaled(WORKLOADS["periodic_large_batch"], name="per
 def _unit_rows(g: torch.Generator, shape, norm: float, device) -> torch.Tensor:
     x = torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
     return x * (norm / x.norm(dim=-1, keepdim=True))
+
+
+def rope_rows(x: torch.Tensor, pos: torch.Tensor, theta: float, style: int = 0) -> torch.Tensor:
+    """The model's RoPE of rows x [..., n, d] at positions pos [n]: band f --
+    (x[2f], x[2f+1]) for style 0, (x[f], x[f+d/2]) for style 1 -- rotated by
+    angle theta^(-2f/d) * pos. Angles in fp64, result in fp32."""
+    d = x.shape[-1]
+    F = d // 2
+    f = torch.arange(F, dtype=torch.float64, device=x.device)
+    omega = torch.pow(torch.tensor(float(theta), dtype=torch.float64, device=x.device), -2.0 * f / d)
+    ang = pos.to(torch.float64)[:, None] * omega[None, :]
+    cs, sn = torch.cos(ang).to(torch.float32), torch.sin(ang).to(torch.float32)
+    x = x.to(torch.float32)
+    if style == 0:
+        a, b = x[..., 0::2], x[..., 1::2]
+    else:
+        a, b = x[..., :F], x[..., F:]
+    ra, rb = a * cs - b * sn, a * sn + b * cs
+    out = torch.empty_like(x)
+    if style == 0:
+        out[..., 0::2], out[..., 1::2] = ra, rb
+    else:
+        out[..., :F], out[..., F:] = ra, rb
+    return out
 
 
 @dataclass
@@ -153,10 +189,14 @@ def make_inputs(w: Workload, device="cuda", with_queries: bool = True, seqs: int
     k = torch.empty(n_seq, L, H, w.n_cap, d, dtype=w.dtype, device=device)
     v = torch.empty_like(k)
     rows = w.n_valid
+    slots = torch.arange(rows, device=device)
     for s in range(n_seq):
         for l in range(L):
             noise = torch.randn(H, rows, d, generator=g, device=device)
-            k[s, l, :, :rows] = (mu_k[l][:, None, :] + w.key_noise_std * noise).to(w.dtype)
+            kk = mu_k[l][:, None, :] + w.key_noise_std * noise
+            if w.key_layout == "post":
+                kk = rope_rows(kk, slots, w.theta)
+            k[s, l, :, :rows] = kk.to(w.dtype)
             v[s, l, :, :rows] = (w.value_std * torch.randn(H, rows, d, generator=g, device=device)).to(w.dtype)
             if rows < w.n_cap:
                 k[s, l, :, rows:] = 0

@@ -53,18 +53,19 @@ def test_status_strings_and_version(lib):
     for code in range(5):
         assert lib.tri_status_string(code)
     assert lib.tri_status_string(99) == b"unknown status"
-    assert lib.tri_abi_version() == 1
+    assert lib.tri_abi_version() == 2
     assert lib.tri_launch_count() >= 0
 
 
 def _kv(**over):
     import kv_cache_compression_tri_gb300 as tri
     f = dict(k=0x10000, v=0x20000, pos=None, pos_out=0x30000, n_valid=0x40000, slice_stride=128 * 64,
-             n_seq=1, n_layers=1, n_kv_heads=2, n_cap=128, head_dim=64, dtype=1, dev_status=None)
+             n_seq=1, n_layers=1, n_kv_heads=2, n_cap=128, head_dim=64, dtype=1, dev_status=None,
+             key_layout=0)
     f.update(over)
     return tri._TriKV(f["k"], f["v"], f["pos"], f["pos_out"], f["n_valid"], f["slice_stride"],
                       f["n_seq"], f["n_layers"], f["n_kv_heads"], f["n_cap"], f["head_dim"], f["dtype"],
-                      f["dev_status"])
+                      f["dev_status"], f["key_layout"])
 
 
 INVALID, UNSUPPORTED = 1, 2
@@ -81,6 +82,7 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(n_cap=0), INVALID),
     (dict(n_seq=0), INVALID),
     (dict(pos_out=None), INVALID),  # compaction needs a position target
+    (dict(key_layout=2), INVALID),  # neither pre- nor post-RoPE
 ])
 def test_compact_rejects_bad_cache(lib, over, code):
     kv = _kv(**over)
@@ -119,6 +121,7 @@ def test_score_rejects_bad_args(lib):
     assert call(p_cur=None) == INVALID
     assert call(scores=None) == INVALID
     assert call(kv=_kv(head_dim=256)) == UNSUPPORTED
+    assert call(kv=_kv(key_layout=-1)) == INVALID
     assert call(c=tri._TriCenters(None, 0x80000, 0x90000)) == INVALID
 
 
@@ -148,3 +151,29 @@ def test_kv_cache_bytes_worked_example(golden):
     from kv_cache_compression_tri_gb300.synth import kv_cache_bytes
     for c in golden("kv_bytes.json")["cases"]:
         assert kv_cache_bytes(c["layers"], c["d_model"], c["tokens"], c["elem_bytes"], c["batch"]) == c["bytes"]
+
+
+def test_gqa_entry_points_reject_bad_args(lib):
+    import kv_cache_compression_tri_gb300 as tri
+    kv = _kv()
+    c = tri._TriCenters(0x70000, 0x80000, 0x90000)
+    offs = (ctypes.c_int32 * 3)(1, 2, 4)
+    op = ctypes.cast(offs, ctypes.c_void_p)
+    ws = lib.tri_score_heads_workspace_bytes(ctypes.byref(kv), 4)
+    assert ws > 0 and ws % 8 == 0
+    assert lib.tri_score_heads_workspace_bytes(ctypes.byref(kv), 9) == 0  # group > 8
+    assert lib.tri_score_heads_workspace_bytes(ctypes.byref(kv), 0) == 0
+    call = lambda **o: lib.tri_score_heads(ctypes.byref(kv), ctypes.byref(c), o.get("group", 4), 1e4, 0, 0, op,
+                                           3, 0xA0000, 0xB0000, o.get("stats", 0xD0000),
+                                           o.get("ws", 0xC0000), o.get("ws_bytes", ws), None)
+    assert call(group=9) == INVALID
+    assert call(stats=None) == INVALID
+    assert call(ws=None) == INVALID
+    assert call(ws_bytes=ws - 1) == INVALID
+    sel = lambda **o: lib.tri_select_topk_zmax(0xB0000, o.get("stats", 0xD0000), o.get("group", 4),
+                                               ctypes.byref(kv), 0, 0, o.get("budget", 64), 0x50000,
+                                               o.get("final", None), None)
+    assert sel(group=0) == INVALID
+    assert sel(stats=None) == INVALID
+    assert sel(budget=129) == INVALID
+    assert sel(final=0xE0002) == INVALID  # misaligned output
