@@ -32,6 +32,10 @@ Parity status of each function (what pins it, all in ``tests/test_oracle_*``):
                         pre-RoPE score of the un-rotated keys.
   score_heads        -- per-query-head scores: score_series once per head;
                         identical heads reduce to the pooled score.
+  union_select       -- brute-force set construction on tiny inputs; with
+                        k_head >= the number kept it reduces to the top by
+                        the z-score maximum, with k_head = 0 likewise; a
+                        single head gives the plain selection.
   zscore_max         -- a hand-worked two-head example in closed form,
                         invariance under a positive affine map of any head,
                         unit variance of every z-scored head, constant heads.
@@ -96,6 +100,8 @@ def _load():
             lib.orc_rand_select.restype = i32
             lib.orc_rope_rows.argtypes = [vp, vp, i64, i64, i32, dbl, i32, vp]
             lib.orc_rope_rows.restype = None
+            lib.orc_union_select.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp, vp, vp]
+            lib.orc_union_select.restype = i32
             lib.orc_zscore_max.argtypes = [vp, i64, i64, vp, vp, vp]
             lib.orc_zscore_max.restype = None
             _lib = lib
@@ -270,3 +276,31 @@ def score_post_rope(k_post, pos, center, mean_norm, mrl, offsets, p_cur: int, th
     k = rope_rows(k_post, pos, theta, style=style, inverse=True)
     return score_series(k, center, mean_norm, mrl, offsets, p_cur, theta, pos=pos, style=style,
                         norm_mode=norm_mode)
+
+
+def rand_select_shared(seed: int, rnd: int, seq: int, layer: int, head: int, scope: int, n_valid: int,
+                       n_prompt: int, n_recent: int, budget: int) -> np.ndarray:
+    """The shared-draw control of Random Attention (Appendix D): every head
+    uses one draw -- head 0's for scope 1 (per layer), layer 0 head 0's for
+    scope 2 (per sequence); scope 0 is the per-head draw."""
+    if scope >= 1:
+        head = 0
+    if scope >= 2:
+        layer = 0
+    return rand_select(seed, rnd, seq, layer, head, n_valid, n_prompt, n_recent, budget)
+
+
+def union_select(scores_h, n_valid: int, n_prompt: int, n_recent: int, budget: int, k_head: int):
+    """One keep list shared by H heads (the blog's union-based selection).
+    scores_h: [H][n]. Returns (keep [budget], member [n] bool, combined [n])."""
+    s = _f64(scores_h)
+    H, n = s.shape
+    assert n == n_valid
+    member = np.zeros(n, dtype=np.int32)
+    combined = np.zeros(n)
+    keep = np.zeros(budget, dtype=np.int32)
+    rc = _load().orc_union_select(_ptr(s), H, n, n_prompt, n_recent, budget, k_head, _ptr(member),
+                                  _ptr(combined), _ptr(keep))
+    if rc != 0:
+        raise ValueError("budget < n_prompt + n_recent")
+    return keep, member.astype(bool), combined

@@ -398,4 +398,57 @@ void orc_zscore_max(const double* scores, int64_t G, int64_t n, double* mean, do
   }
 }
 
+// ---------------------------------------------------------------------------
+// Union-based selection across heads ([TB] "eviction (union-based
+// selection)"): the H heads that must share one keep-set (here the KV heads
+// of one (seq, layer)) each pick their own top candidates; the union of those
+// picks is kept first, ranked by a combined score, and if it holds fewer than
+// the budget the rest is filled by the combined score.
+// Readings: each head picks its top k_head candidates (score desc, slot asc,
+// NaN lowest); the combined score is [TA]'s normalise-then-max (per-head
+// z-score over all n rows, population std, then the maximum over heads, as
+// orc_zscore_max); the final order is (in the union first, combined score
+// desc, slot asc); prompt [0, P) and recent [n - W, n) are kept as in
+// orc_select. scores: [H][n]. member: [n] out (1 = in the union), combined:
+// [n] out, keep: [B] out. Returns 0, or -1 when B < P + W and eviction is
+// needed.
+// ---------------------------------------------------------------------------
+int orc_union_select(const double* scores, int64_t H, int64_t n, int64_t P, int64_t W, int64_t B,
+                     int64_t k_head, int32_t* member, double* combined, int32_t* keep) {
+  std::vector<double> mean(H), stdev(H);
+  orc_zscore_max(scores, H, n, mean.data(), stdev.data(), combined);
+  for (int64_t i = 0; i < n; ++i) member[i] = 0;
+  if (n <= B) {
+    for (int64_t j = 0; j < B; ++j) keep[j] = (j < n) ? static_cast<int32_t>(j) : -1;
+    return 0;
+  }
+  if (B < P + W) return -1;
+  auto higher = [](double a, double b) {  // a ranks above b; NaN lowest
+    if (std::isnan(a)) return false;
+    if (std::isnan(b)) return true;
+    return a > b;
+  };
+  std::vector<int64_t> cand;
+  for (int64_t i = P; i < n - W; ++i) cand.push_back(i);
+  for (int64_t h = 0; h < H; ++h) {
+    const double* s = scores + h * n;
+    std::vector<int64_t> order = cand;
+    std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return higher(s[a], s[b]); });
+    const int64_t take = std::min<int64_t>(k_head, static_cast<int64_t>(order.size()));
+    for (int64_t j = 0; j < take; ++j) member[order[j]] = 1;
+  }
+  std::vector<int64_t> order = cand;
+  std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+    if (member[a] != member[b]) return member[a] > member[b];
+    return higher(combined[a], combined[b]);
+  });
+  std::vector<int64_t> kept;
+  for (int64_t i = 0; i < P; ++i) kept.push_back(i);
+  for (int64_t j = 0; j < B - P - W; ++j) kept.push_back(order[j]);
+  for (int64_t i = n - W; i < n; ++i) kept.push_back(i);
+  std::sort(kept.begin(), kept.end());
+  for (int64_t j = 0; j < B; ++j) keep[j] = static_cast<int32_t>(kept[j]);
+  return 0;
+}
+
 }  // extern "C"

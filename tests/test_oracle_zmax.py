@@ -71,3 +71,65 @@ def test_identical_heads_reduce_to_the_pooled_score():
     assert np.array_equal(heads[0], pooled) and np.array_equal(heads[1], pooled)
     _, _, final = orc.zscore_max(heads)
     assert np.array_equal(orc.select(final, n, 8, 16, 100), orc.select(pooled, n, 8, 16, 100))
+
+
+# ---- union-based selection across heads --------------------------------------
+def _brute_union(s, n, P, W, B, k):
+    """Direct set construction: each head's top-k candidates (stable by slot),
+    their union ranked by the z-score maximum, then the rest by it."""
+    H = s.shape[0]
+    cand = list(range(P, n - W))
+    _, _, comb = orc.zscore_max(s)
+    union = set()
+    for h in range(H):
+        ranked = sorted(cand, key=lambda i: (-s[h, i], i))
+        union |= set(ranked[:k])
+    need = B - P - W
+    in_u = sorted(union, key=lambda i: (-comb[i], i))
+    rest = sorted(set(cand) - union, key=lambda i: (-comb[i], i))
+    chosen = (in_u + rest)[:need]
+    return sorted(list(range(P)) + chosen + list(range(n - W, n)))
+
+
+def test_union_select_brute_force():
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        H, n = int(rng.integers(1, 5)), int(rng.integers(20, 80))
+        s = np.round(rng.normal(size=(H, n)) * 3) / 3 * rng.uniform(0.5, 5, size=(H, 1))  # ties, scales
+        P, W = int(rng.integers(0, 5)), int(rng.integers(0, 5))
+        B = int(rng.integers(P + W + 1, n))
+        k = int(rng.integers(0, n))
+        keep, member, comb = orc.union_select(s, n, P, W, B, k)
+        assert keep.tolist() == _brute_union(s, n, P, W, B, k), trial
+        assert member.sum() <= H * k
+
+
+def test_union_select_reductions():
+    rng = np.random.default_rng(6)
+    s = rng.normal(size=(4, 300)) * [[1], [3], [0.5], [2]]
+    n, P, W, B = 300, 10, 20, 100
+    need = B - P - W
+    _, _, comb = orc.zscore_max(s)
+    top = orc.select(comb, n, P, W, B)
+    # every head keeps >= need of its own: the union holds the top by the maximum
+    assert np.array_equal(orc.union_select(s, n, P, W, B, need)[0], top)
+    # an empty union: filled by the combined score alone
+    assert np.array_equal(orc.union_select(s, n, P, W, B, 0)[0], top)
+    # one head: the plain selection on its score, whatever k
+    for k in (0, 5, need, 200):
+        assert np.array_equal(orc.union_select(s[1:2], n, P, W, B, k)[0], orc.select(s[1], n, P, W, B))
+    # a small k changes the result: union members beat higher combined scores
+    keep_small = orc.union_select(s, n, P, W, B, 3)[0]
+    assert len(set(keep_small.tolist())) == B
+    # nothing to evict
+    assert orc.union_select(s[:, :90], 90, P, W, B, 3)[0].tolist() == list(range(90)) + [-1] * 10
+
+
+def test_shared_draw_is_one_keep_set_for_every_head():
+    a = [orc.rand_select_shared(3, 1, 0, 2, h, 1, 900, 50, 0, 300) for h in range(4)]
+    assert all(np.array_equal(a[0], x) for x in a)
+    assert np.array_equal(a[0], orc.rand_select(3, 1, 0, 2, 0, 900, 50, 0, 300))
+    b = orc.rand_select_shared(3, 1, 0, 2, 3, 2, 900, 50, 0, 300)
+    assert np.array_equal(b, orc.rand_select(3, 1, 0, 0, 0, 900, 50, 0, 300))
+    assert np.array_equal(orc.rand_select_shared(3, 1, 0, 2, 3, 0, 900, 50, 0, 300),
+                          orc.rand_select(3, 1, 0, 2, 3, 900, 50, 0, 300))
