@@ -102,6 +102,10 @@ def _load():
             lib.orc_rope_rows.restype = None
             lib.orc_union_select.argtypes = [vp, i64, i64, i64, i64, i64, i64, vp, vp, vp]
             lib.orc_union_select.restype = i32
+            lib.orc_union_members.argtypes = [vp, i64, i64, i64, i64, i64, vp]
+            lib.orc_union_members.restype = None
+            lib.orc_union_rank.argtypes = [vp, vp, i64, i64, i64, i64, vp]
+            lib.orc_union_rank.restype = i32
             lib.orc_zscore_max.argtypes = [vp, i64, i64, vp, vp, vp]
             lib.orc_zscore_max.restype = None
             _lib = lib
@@ -304,3 +308,23 @@ def union_select(scores_h, n_valid: int, n_prompt: int, n_recent: int, budget: i
     if rc != 0:
         raise ValueError("budget < n_prompt + n_recent")
     return keep, member.astype(bool), combined
+
+
+def union_members(scores_h, n_prompt: int, n_recent: int, k_head: int) -> np.ndarray:
+    """Step 1 of union_select: the union of every head's top k_head candidates."""
+    s = _f64(scores_h)
+    H, n = s.shape
+    member = np.zeros(n, dtype=np.int32)
+    _load().orc_union_members(_ptr(s), H, n, n_prompt, n_recent, k_head, _ptr(member))
+    return member.astype(bool)
+
+
+def union_rank(member, combined, n_prompt: int, n_recent: int, budget: int) -> np.ndarray:
+    """Step 2 of union_select: members first by the combined score, then the rest."""
+    m = np.ascontiguousarray(np.asarray(member, dtype=np.int32))
+    c = _f64(combined)
+    keep = np.zeros(budget, dtype=np.int32)
+    rc = _load().orc_union_rank(_ptr(m), _ptr(c), len(c), n_prompt, n_recent, budget, _ptr(keep))
+    if rc != 0:
+        raise ValueError("budget < n_prompt + n_recent")
+    return keep

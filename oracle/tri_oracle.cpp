@@ -413,34 +413,45 @@ void orc_zscore_max(const double* scores, int64_t G, int64_t n, double* mean, do
 // [n] out, keep: [B] out. Returns 0, or -1 when B < P + W and eviction is
 // needed.
 // ---------------------------------------------------------------------------
-int orc_union_select(const double* scores, int64_t H, int64_t n, int64_t P, int64_t W, int64_t B,
-                     int64_t k_head, int32_t* member, double* combined, int32_t* keep) {
-  std::vector<double> mean(H), stdev(H);
-  orc_zscore_max(scores, H, n, mean.data(), stdev.data(), combined);
+namespace {
+bool ranks_higher(double a, double b) {  // a above b; NaN lowest
+  if (std::isnan(a)) return false;
+  if (std::isnan(b)) return true;
+  return a > b;
+}
+}  // namespace
+
+// Step 1: the union of every head's top k_head candidates [P, n - W) by its
+// own score (score desc, slot asc, NaN lowest). member: [n] out.
+void orc_union_members(const double* scores, int64_t H, int64_t n, int64_t P, int64_t W, int64_t k_head,
+                       int32_t* member) {
   for (int64_t i = 0; i < n; ++i) member[i] = 0;
-  if (n <= B) {
-    for (int64_t j = 0; j < B; ++j) keep[j] = (j < n) ? static_cast<int32_t>(j) : -1;
-    return 0;
-  }
-  if (B < P + W) return -1;
-  auto higher = [](double a, double b) {  // a ranks above b; NaN lowest
-    if (std::isnan(a)) return false;
-    if (std::isnan(b)) return true;
-    return a > b;
-  };
   std::vector<int64_t> cand;
   for (int64_t i = P; i < n - W; ++i) cand.push_back(i);
   for (int64_t h = 0; h < H; ++h) {
     const double* s = scores + h * n;
     std::vector<int64_t> order = cand;
-    std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return higher(s[a], s[b]); });
+    std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return ranks_higher(s[a], s[b]); });
     const int64_t take = std::min<int64_t>(k_head, static_cast<int64_t>(order.size()));
     for (int64_t j = 0; j < take; ++j) member[order[j]] = 1;
   }
-  std::vector<int64_t> order = cand;
+}
+
+// Step 2: keep [0, P), then B - P - W candidates in the order (member first,
+// combined desc with NaN lowest, slot asc), then [n - W, n); ascending.
+// Returns 0, or -1 when B < P + W and eviction is needed.
+int orc_union_rank(const int32_t* member, const double* combined, int64_t n, int64_t P, int64_t W, int64_t B,
+                   int32_t* keep) {
+  if (n <= B) {
+    for (int64_t j = 0; j < B; ++j) keep[j] = (j < n) ? static_cast<int32_t>(j) : -1;
+    return 0;
+  }
+  if (B < P + W) return -1;
+  std::vector<int64_t> order;
+  for (int64_t i = P; i < n - W; ++i) order.push_back(i);
   std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
     if (member[a] != member[b]) return member[a] > member[b];
-    return higher(combined[a], combined[b]);
+    return ranks_higher(combined[a], combined[b]);
   });
   std::vector<int64_t> kept;
   for (int64_t i = 0; i < P; ++i) kept.push_back(i);
@@ -449,6 +460,19 @@ int orc_union_select(const double* scores, int64_t H, int64_t n, int64_t P, int6
   std::sort(kept.begin(), kept.end());
   for (int64_t j = 0; j < B; ++j) keep[j] = static_cast<int32_t>(kept[j]);
   return 0;
+}
+
+// Both steps, with the combined score of orc_zscore_max.
+int orc_union_select(const double* scores, int64_t H, int64_t n, int64_t P, int64_t W, int64_t B,
+                     int64_t k_head, int32_t* member, double* combined, int32_t* keep) {
+  std::vector<double> mean(H), stdev(H);
+  orc_zscore_max(scores, H, n, mean.data(), stdev.data(), combined);
+  if (n <= B) {
+    for (int64_t i = 0; i < n; ++i) member[i] = 0;
+  } else {
+    orc_union_members(scores, H, n, P, W, k_head, member);
+  }
+  return orc_union_rank(member, combined, n, P, W, B, keep);
 }
 
 }  // extern "C"

@@ -133,3 +133,11 @@ def test_shared_draw_is_one_keep_set_for_every_head():
     assert np.array_equal(b, orc.rand_select(3, 1, 0, 0, 0, 900, 50, 0, 300))
     assert np.array_equal(orc.rand_select_shared(3, 1, 0, 2, 3, 0, 900, 50, 0, 300),
                           orc.rand_select(3, 1, 0, 2, 3, 900, 50, 0, 300))
+
+
+def test_union_steps_compose():
+    rng = np.random.default_rng(7)
+    s = rng.normal(size=(3, 200)) * [[1], [4], [2]]
+    keep, member, comb = orc.union_select(s, 200, 5, 7, 80, 10)
+    assert np.array_equal(orc.union_members(s, 5, 7, 10), member)
+    assert np.array_equal(orc.union_rank(member, comb, 5, 7, 80), keep)
