@@ -578,6 +578,54 @@ def measure_other(args, tri, synth, dev):
     del inp, kh, vh, kv, keep, scores_g, stats, hws
     torch.cuda.empty_cache()
 
+    # ---- the stack with one keep list per (seq, layer): union across heads ---
+    w = synth.WORKLOADS["qwen3_8b_stack"]
+    S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    k_head = B - P - W  # every head picks as many as are kept
+    inp = synth.make_inputs(w, dev)
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    torch.cuda.empty_cache()
+    kh, vh = inp.k[:, :, :, :B].clone(), inp.v[:, :, :, :B].clone()
+    nv = torch.full((S,), n, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = tri.KVCache(inp.k, inp.v, nv, None, torch.empty(S, w.n_cap, dtype=torch.int32, device=dev), st)
+    scores = torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+    uws = torch.empty(tri.select_union_workspace_bytes(kv, P, W, k_head), dtype=torch.uint8, device=dev)
+    kms = []
+
+    def union_event():
+        e = [ev() for _ in range(4)]
+        e[0].record()
+        tri.score(kv, c, w.theta, w.offsets, inp.p_cur, scores)  # the statistics need every row
+        e[1].record()
+        tri.select_union(scores, kv, P, W, B, k_head, keep, workspace=uws)
+        e[2].record()
+        tri.compact_kv(kv, keep, B)
+        e[3].record()
+        kms.append(e)
+
+    def restore_u():
+        inp.k[:, :, :, :B].copy_(kh)
+        inp.v[:, :, :, :B].copy_(vh)
+        nv.fill_(n)
+
+    ms = timed(union_event, restore_u)
+    kt = [[x[0].elapsed_time(x[1]), x[1].elapsed_time(x[2]), x[2].elapsed_time(x[3])] for x in kms[args.warmup:]]
+    k_ms = [sum(x[j] for x in kt) / len(kt) for j in range(3)]
+    moved = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
+    score_by = S * n * w.head_dim * w.elem_bytes
+    by = score_by + moved * (4 * w.head_dim * w.elem_bytes + 8)
+    assert int(st.item()) == 0
+    out["qwen3_8b_stack_union"] = {
+        "value": S * n / (ms / 1e3), "unit": UNIT, "ms_per_event": ms, "gbs": by / ms / 1e6,
+        "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
+        "algorithmic_bytes": by, "k_head": k_head, "heads_per_list": w.n_kv_heads,
+        "kernel_ms": {"score": round(k_ms[0], 4), "select_union": round(k_ms[1], 4), "compact": round(k_ms[2], 4)}}
+    del inp, kh, vh, kv, keep, scores, uws
+    torch.cuda.empty_cache()
+
     # ---- the stack with post-RoPE keys (the engine layout) ------------------
     w = synth.WORKLOADS["qwen3_8b_stack_post_rope"]
     S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget

@@ -62,6 +62,7 @@ typedef enum {
 #define TRI_DEV_NAN_SCORE 2       /* a candidate score was NaN (ranked lowest)    */
 #define TRI_DEV_BAD_KEEP 3        /* keep list not ascending / out of range       */
 #define TRI_DEV_TIMEOUT 4         /* a bounded in-kernel wait gave up (~2 s)      */
+#define TRI_DEV_GROUP_NVALID 5    /* slices sharing a keep list differ in n_valid */
 
 typedef enum { TRI_F32 = 0, TRI_BF16 = 1 } tri_dtype;
 
@@ -245,6 +246,20 @@ tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n
                       tri_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * rand_evict_scoped -- rand_evict with the draw shared across heads: [RA]
+ * Appendix D's shared-draw control keeps the prompt and uses ONE random
+ * keep-set for every head (no cross-head diversity). Scope PER_HEAD is
+ * rand_evict; PER_LAYER gives every KV head of a (seq, layer) the draw of
+ * head 0 (counter word 1 = 65536 * layer); PER_SEQUENCE gives every head of
+ * every layer the draw of (layer 0, head 0) (counter word 1 = 0). Slices that
+ * share a draw and have the same n_valid get identical keep lists.
+ * ------------------------------------------------------------------------ */
+typedef enum { TRI_DRAW_PER_HEAD = 0, TRI_DRAW_PER_LAYER = 1, TRI_DRAW_PER_SEQUENCE = 2 } tri_draw_scope;
+tri_status rand_evict_scoped(const tri_kv* kv, uint64_t seed, uint32_t round, tri_draw_scope scope,
+                             int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                             tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * tri_compress -- one compression event: score + select + compact.
  * Exactly tri_score (rows [n_prompt, n_valid - n_recent)), tri_select_topk
  * and tri_compact_kv called in sequence with the same arguments (three
@@ -297,6 +312,33 @@ tri_status tri_select_topk_zmax(const float* scores_g, const float* stats, int32
                                 const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
                                 int32_t budget, int32_t* keep_idx, float* final_scores,
                                 tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tri_select_union -- one keep list for the n_kv_heads KV heads of each
+ * (seq, layer): union-based selection ([TB] "eviction (union-based
+ * selection)"):
+ *   1. every head h picks its own top k_head candidates by its own score
+ *      (as tri_select_topk with budget n_prompt + n_recent + k_head);
+ *   2. U = the union of those picks;
+ *   3. the B - n_prompt - n_recent kept candidates are U's best by the
+ *      combined score, or all of U and the best of the rest when U is smaller;
+ *   4. plus [0, n_prompt) and [n - n_recent, n); ascending.
+ * Combined score (a reading; the page leaves it open): [TA]'s normalise-then-
+ * max, c(i) = max_h (s_h(i) - mean_h) / std_h with mean and population std of
+ * each head's scores over all n valid rows (a head with std 0 gives 0),
+ * computed in fp32 as (x - mean) * (1 / std); order (in U first, c desc,
+ * slot asc). scores: [n_slices][n_cap], EVERY valid row scored (tri_score
+ * with n_prompt = n_recent = 0). All heads of a (seq, layer) must hold the
+ * same n_valid (else TRI_DEV_GROUP_NVALID). n_kv_heads: 1..8; n_cap <=
+ * 524288. keep_idx: [n_slices][budget], identical rows within a group.
+ * final_scores: optional [n_seq * n_layers][n_cap], c(i) of every valid row.
+ * ws: tri_select_union_workspace_bytes(kv, n_prompt, n_recent, k_head) bytes,
+ * 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t tri_select_union_workspace_bytes(const tri_kv* kv, int32_t n_prompt, int32_t n_recent, int32_t k_head);
+tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
+                            int32_t budget, int32_t k_head, int32_t* keep_idx, float* final_scores, void* ws,
+                            size_t ws_bytes, tri_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ __all__ = [
     "TriError", "KVCache", "Centers", "lib_path", "load_library", "calibrate_centers",
     "calibrate_workspace_bytes", "score", "select_topk", "compact_kv", "rand_evict",
     "compress", "compress_workspace_bytes", "score_heads", "score_heads_workspace_bytes",
-    "select_topk_zmax",
+    "select_topk_zmax", "select_union", "select_union_workspace_bytes", "rand_evict_scoped", "DRAW_PER_HEAD", "DRAW_PER_LAYER", "DRAW_PER_SEQUENCE",
     "launch_count", "ROPE_INTERLEAVED", "ROPE_HALF", "NORM_WEIGHTED", "NORM_UNWEIGHTED",
     "DEV_OK", "DEV_NVALID_OVER_CAP", "DEV_NAN_SCORE", "DEV_BAD_KEEP",
 ]
@@ -30,7 +30,7 @@ __all__ = [
 ROPE_INTERLEAVED, ROPE_HALF = 0, 1
 NORM_WEIGHTED, NORM_UNWEIGHTED = 0, 1
 F32, BF16 = 0, 1
-DEV_OK, DEV_NVALID_OVER_CAP, DEV_NAN_SCORE, DEV_BAD_KEEP = 0, 1, 2, 3
+DEV_OK, DEV_NVALID_OVER_CAP, DEV_NAN_SCORE, DEV_BAD_KEEP, DEV_TIMEOUT, DEV_GROUP_NVALID = 0, 1, 2, 3, 4, 5
 
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -95,6 +95,8 @@ def load_library():
         lib.tri_compact_kv.restype = ctypes.c_int
         lib.rand_evict.argtypes = [kvp, u64, u32, i32, i32, i32, vp, vp]
         lib.rand_evict.restype = ctypes.c_int
+        lib.rand_evict_scoped.argtypes = [kvp, u64, u32, ctypes.c_int, i32, i32, i32, vp, vp]
+        lib.rand_evict_scoped.restype = ctypes.c_int
         lib.tri_compress_workspace_bytes.argtypes = [kvp]
         lib.tri_compress_workspace_bytes.restype = ctypes.c_size_t
         lib.tri_compress.argtypes = [kvp, ctypes.POINTER(_TriCenters), ctypes.c_double, ctypes.c_int,
@@ -107,6 +109,10 @@ def load_library():
         lib.tri_score_heads.restype = ctypes.c_int
         lib.tri_select_topk_zmax.argtypes = [vp, vp, i32, kvp, i32, i32, i32, vp, vp, vp]
         lib.tri_select_topk_zmax.restype = ctypes.c_int
+        lib.tri_select_union_workspace_bytes.argtypes = [kvp, i32, i32, i32]
+        lib.tri_select_union_workspace_bytes.restype = ctypes.c_size_t
+        lib.tri_select_union.argtypes = [vp, kvp, i32, i32, i32, i32, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.tri_select_union.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -255,6 +261,21 @@ def rand_evict(kv: KVCache, seed: int, rnd: int, n_prompt: int, n_recent: int, b
     return keep
 
 
+DRAW_PER_HEAD, DRAW_PER_LAYER, DRAW_PER_SEQUENCE = 0, 1, 2
+
+
+def rand_evict_scoped(kv: KVCache, seed: int, rnd: int, scope: int, n_prompt: int, n_recent: int, budget: int,
+                      keep: torch.Tensor, stream=None) -> torch.Tensor:
+    """Random Attention keep lists with the draw shared by every KV head of a
+    layer (DRAW_PER_LAYER) or of a sequence (DRAW_PER_SEQUENCE) (rand_evict_scoped)."""
+    lib = load_library()
+    assert keep.dtype == torch.int32 and keep.is_contiguous() and keep.numel() == kv.n_slices * budget
+    kvs = kv._abi()
+    _check("rand_evict_scoped", lib.rand_evict_scoped(ctypes.byref(kvs), seed, rnd, scope, n_prompt, n_recent,
+                                                      budget, keep.data_ptr(), _stream(stream)))
+    return keep
+
+
 def compact_kv(kv: KVCache, keep: torch.Tensor, budget: int, stream=None) -> None:
     """In-place order-preserving compaction of K, V and positions (tri_compact_kv)."""
     lib = load_library()
@@ -333,4 +354,30 @@ def select_topk_zmax(scores_g: torch.Tensor, stats: torch.Tensor, group: int, kv
     _check("tri_select_topk_zmax", lib.tri_select_topk_zmax(
         scores_g.data_ptr(), stats.data_ptr(), group, ctypes.byref(kvs), n_prompt, n_recent, budget,
         keep.data_ptr(), _ptr(final_scores), _stream(stream)))
+    return keep
+
+
+def select_union_workspace_bytes(kv: KVCache, n_prompt: int, n_recent: int, k_head: int) -> int:
+    kvs = kv._abi()
+    return int(load_library().tri_select_union_workspace_bytes(ctypes.byref(kvs), n_prompt, n_recent, k_head))
+
+
+def select_union(scores: torch.Tensor, kv: KVCache, n_prompt: int, n_recent: int, budget: int, k_head: int,
+                 keep: torch.Tensor, final_scores: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One keep list per (seq, layer) shared by its KV heads: union of every
+    head's top k_head, ranked by the z-score maximum, topped up by it
+    (tri_select_union). `scores` must cover every valid row."""
+    lib = load_library()
+    assert keep.dtype == torch.int32 and keep.is_contiguous() and keep.numel() == kv.n_slices * budget
+    kvs = kv._abi()
+    need = int(lib.tri_select_union_workspace_bytes(ctypes.byref(kvs), n_prompt, n_recent, k_head))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=kv.k.device)
+    assert workspace.numel() >= need
+    if final_scores is not None:
+        assert final_scores.dtype == torch.float32 and final_scores.is_contiguous()
+    _check("tri_select_union", lib.tri_select_union(
+        scores.data_ptr(), ctypes.byref(kvs), n_prompt, n_recent, budget, k_head, keep.data_ptr(),
+        _ptr(final_scores), workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return keep

@@ -342,11 +342,11 @@ __global__ void heads_stats_kernel(const double* __restrict__ partials, float* _
 // The final score max_g z_g of every valid row (for callers that want the
 // values; the selection computes them on the fly in the same way).
 __global__ void zmax_scores_kernel(const float* __restrict__ scores_g, const float* __restrict__ stats,
-                                   const int32_t* __restrict__ n_valid, float* __restrict__ out, int n_cap,
-                                   int group, int blocks_per_slice) {
+                                   const int32_t* __restrict__ n_valid, int nv_stride, float* __restrict__ out,
+                                   int n_cap, int group, int blocks_per_slice) {
   const int64_t s = blockIdx.x / blocks_per_slice;
   const int i = (blockIdx.x % blocks_per_slice) * blockDim.x + threadIdx.x;
-  const int n = min(n_valid[s], n_cap);
+  const int n = min(n_valid[s * nv_stride], n_cap);
   if (i >= n) return;
   float best = 0.f;
   for (int g = 0; g < group; ++g) {
@@ -416,12 +416,13 @@ cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slice
   return cudaGetLastError();
 }
 
-cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid,
-                               float* out, int n_slices, int n_cap, int group, cudaStream_t st) {
+cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid, int nv_stride,
+                               float* out, int n_blocks, int n_cap, int group, cudaStream_t st) {
   const int bps = (n_cap + 255) / 256;
-  const int64_t blocks = static_cast<int64_t>(bps) * n_slices;
+  const int64_t blocks = static_cast<int64_t>(bps) * n_blocks;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  zmax_scores_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(scores_g, stats, n_valid, out, n_cap, group, bps);
+  zmax_scores_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(scores_g, stats, n_valid, nv_stride, out,
+                                                                     n_cap, group, bps);
   note_launch();
   return cudaGetLastError();
 }

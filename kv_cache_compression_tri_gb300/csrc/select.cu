@@ -278,6 +278,7 @@ __device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const K
 // fp32 scores [S][n_cap]; keys of slots outside [P, end) read as 0.
 struct ScoreKeys {
   static constexpr int U = 4;  // 16-byte loads in flight per thread
+  static constexpr bool GROUPED = false;
   const float* row;
   bool vec;  // 16-byte loads allowed
 
@@ -317,11 +318,16 @@ struct ScoreKeys {
 // Philox-4x32-10 draws (Salmon et al., SC'11).
 struct DrawKeys {
   static constexpr int U = 1;
+  static constexpr bool GROUPED = false;
   uint4 ctr;  // counter words 1..3 (head + 65536 layer, seq, round)
   uint2 key;
 
   __device__ static DrawKeys make(const SelectParams& p, const Ctx&, int seq, int layer, int head) {
     DrawKeys k;
+    // a shared draw (Random Attention, Appendix D's control) is the draw of
+    // head 0 (of layer 0 for a whole sequence) used by every head
+    if (p.draw_scope >= 1) head = 0;
+    if (p.draw_scope >= 2) layer = 0;
     k.ctr = make_uint4(0u, static_cast<uint32_t>(head + 65536 * layer), static_cast<uint32_t>(seq), p.round);
     k.key = make_uint2(static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
     return k;
@@ -352,23 +358,26 @@ struct DrawKeys {
 template <int G>
 struct ZMaxKeys {
   static constexpr int U = 1;
-  const float* base;  // this slice's head 0 row
+  static constexpr bool GROUPED = false;
+  const float* base;  // row 0 of the G score rows
   int64_t n_cap;
   float mu[G], inv[G];
   bool vec;
 
-  __device__ static ZMaxKeys make(const SelectParams& p, const Ctx& c, int, int, int) {
+  // score rows [block * G, block * G + G) and their statistics
+  __device__ static ZMaxKeys at(const SelectParams& p, int64_t block) {
     ZMaxKeys k;
     k.n_cap = p.n_cap;
-    k.base = p.scores + c.s * G * k.n_cap;
+    k.base = p.scores + block * G * k.n_cap;
     k.vec = (reinterpret_cast<uintptr_t>(k.base) & 15) == 0 && (p.n_cap & 3) == 0;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      k.mu[g] = p.stats[(c.s * G + g) * 2];
-      k.inv[g] = head_inv_std(p.stats[(c.s * G + g) * 2 + 1]);
+      k.mu[g] = p.stats[(block * G + g) * 2];
+      k.inv[g] = head_inv_std(p.stats[(block * G + g) * 2 + 1]);
     }
     return k;
   }
+  __device__ static ZMaxKeys make(const SelectParams& p, const Ctx& c, int, int, int) { return at(p, c.s); }
   __device__ __forceinline__ float final_score(int slot) const {
     float best = 0.f;
 #pragma unroll
@@ -378,8 +387,8 @@ struct ZMaxKeys {
     }
     return best;
   }
-  __device__ __forceinline__ uint4 fetch(int i0, int P, int end, bool& nan) const {
-    float best[4];
+  // max_g z_g of slots i0 .. i0+3 (those < end; i0 a multiple of 4)
+  __device__ __forceinline__ void best4(int i0, int end, float (&best)[4]) const {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float* row = base + g * n_cap;
@@ -400,6 +409,10 @@ struct ZMaxKeys {
         best[e] = (g == 0) ? z : fmaxf(best[e], z);
       }
     }
+  }
+  __device__ __forceinline__ uint4 fetch(int i0, int P, int end, bool& nan) const {
+    float best[4];
+    best4(i0, end, best);
     uint32_t k[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) k[e] = in_range(i0 + e, P, end) ? score_key(best[e], nan) : 0u;
@@ -410,6 +423,54 @@ struct ZMaxKeys {
     sampled_window(sm, c, need, m, [&self](int slot) {
       bool ignored = false;
       return score_key(self.final_score(slot), ignored);
+    }, t_lo, t_hi);
+  }
+};
+
+// Union-based selection across the H KV heads of a (seq, layer) (the
+// TriAttention blog, "eviction (union-based selection)"): one keep list for
+// the group. Candidates in the union of the heads' own top picks rank first,
+// each group by the combined score max_h z_h (ZMaxKeys over the group's H
+// score rows). Encoded in one u32 key: when the union holds at least `need`
+// candidates only members compete (members: the score's order key, at least
+// 1; others 0); otherwise every member is kept (key all ones) and the others
+// compete by the combined score.
+template <int H>
+struct UnionKeys {
+  static constexpr int U = 1;
+  static constexpr bool GROUPED = true;
+  ZMaxKeys<H> z;
+  const uint32_t* member;  // the group's union bitmap, bit i = slot i
+  bool many;
+
+  __device__ static UnionKeys make(const SelectParams& p, const Ctx& c, int, int, int) {
+    UnionKeys k;
+    const int64_t group = c.s / H;
+    k.z = ZMaxKeys<H>::at(p, group);
+    k.member = p.member + group * p.member_words;
+    k.many = p.ucount[group] >= c.B - c.P - c.W;
+    return k;
+  }
+  __device__ __forceinline__ uint32_t key(bool in_union, float comb, bool& nan) const {
+    const uint32_t k = score_key(comb, nan);
+    if (many) return in_union ? max(k, 1u) : 0u;
+    return in_union ? 0xffffffffu : k;
+  }
+  __device__ __forceinline__ uint4 fetch(int i0, int P, int end, bool& nan) const {
+    float best[4];
+    z.best4(i0, end, best);
+    const uint32_t word = __ldg(member + (i0 >> 5)) >> (i0 & 31);  // i0 % 4 == 0: one word
+    uint32_t k[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) k[e] = in_range(i0 + e, P, end) ? key((word >> e) & 1u, best[e], nan) : 0u;
+    return make_uint4(k[0], k[1], k[2], k[3]);
+  }
+  __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
+    const UnionKeys& self = *this;
+    sampled_window(sm, c, need, m, [&self](int slot) {
+      bool ignored = false;
+      const bool in_union = (__ldg(self.member + (slot >> 5)) >> (slot & 31)) & 1u;
+      return self.key(in_union, self.z.final_score(slot), ignored);
     }, t_lo, t_hi);
   }
 };
@@ -459,13 +520,13 @@ __device__ void radix_select(SSmem& sm, const Src& src, const Ctx& c, bool from_
   }
 }
 
+// The keep list of slice s (row s of p.keep), by the whole CTA. Every branch
+// that returns early is uniform over the CTA.
 template <class Src>
-__global__ void __launch_bounds__(NT, MINB) select_kernel(const __grid_constant__ SelectParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SSmem& sm = *reinterpret_cast<SSmem*>(smem_raw);
+__device__ __forceinline__ void select_slice(const SelectParams& p, SSmem& sm, int64_t s) {
   const int t = threadIdx.x, lane = t & 31;
   Ctx c;
-  c.s = blockIdx.x;
+  c.s = s;
   c.n = p.n_valid[c.s];
   c.P = p.n_prompt;
   c.W = p.n_recent;
@@ -684,6 +745,25 @@ __global__ void __launch_bounds__(NT, MINB) select_kernel(const __grid_constant_
   if (t == 0 && sm.nan_seen) set_status(p.dev_status, TRI_DEV_NAN_SCORE);
 }
 
+// One CTA per slice, or per group of p.group consecutive slices for a key
+// source whose keep list is shared (Src::GROUPED): the group's first slice is
+// selected and its list copied to the others.
+template <class Src>
+__global__ void __launch_bounds__(NT, MINB) select_kernel(const __grid_constant__ SelectParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SSmem& sm = *reinterpret_cast<SSmem*>(smem_raw);
+  const int64_t s = Src::GROUPED ? static_cast<int64_t>(blockIdx.x) * p.group : blockIdx.x;
+  select_slice<Src>(p, sm, s);
+  if (Src::GROUPED) {
+    __syncthreads();
+    const int32_t* k0 = p.keep + s * static_cast<int64_t>(p.budget);
+    for (int h = 1; h < p.group; ++h) {
+      int32_t* kh = p.keep + (s + h) * static_cast<int64_t>(p.budget);
+      for (int j = threadIdx.x; j < p.budget; j += NT) kh[j] = k0[j];
+    }
+  }
+}
+
 template <class Src>
 cudaError_t launch_src(const SelectParams& p, int n_slices, cudaStream_t st) {
   // The dynamic shared memory opt-in is a per-device function attribute;
@@ -704,6 +784,20 @@ cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st) 
 
 cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st) {
   return launch_src<DrawKeys>(p, n_slices, st);
+}
+
+cudaError_t launch_select_union(const SelectParams& p, int n_groups, cudaStream_t st) {
+  switch (p.group) {
+    case 1: return launch_src<UnionKeys<1>>(p, n_groups, st);
+    case 2: return launch_src<UnionKeys<2>>(p, n_groups, st);
+    case 3: return launch_src<UnionKeys<3>>(p, n_groups, st);
+    case 4: return launch_src<UnionKeys<4>>(p, n_groups, st);
+    case 5: return launch_src<UnionKeys<5>>(p, n_groups, st);
+    case 6: return launch_src<UnionKeys<6>>(p, n_groups, st);
+    case 7: return launch_src<UnionKeys<7>>(p, n_groups, st);
+    case 8: return launch_src<UnionKeys<8>>(p, n_groups, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_select_zmax(const SelectParams& p, int n_slices, cudaStream_t st) {

@@ -7,6 +7,7 @@
 // from rope_theta and the offset set), computed in fp64.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -296,7 +297,15 @@ tri_status tri_select_topk(const float* scores, const tri_kv* kv, int32_t n_prom
 
 tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n_prompt,
                       int32_t n_recent, int32_t budget, int32_t* keep_idx, tri_stream_t stream) {
+  return rand_evict_scoped(kv, seed, round, TRI_DRAW_PER_HEAD, n_prompt, n_recent, budget, keep_idx, stream);
+}
+
+tri_status rand_evict_scoped(const tri_kv* kv, uint64_t seed, uint32_t round, tri_draw_scope scope,
+                             int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                             tri_stream_t stream) {
   if (!kv) return TRI_ERR_INVALID_ARG;
+  if (scope != TRI_DRAW_PER_HEAD && scope != TRI_DRAW_PER_LAYER && scope != TRI_DRAW_PER_SEQUENCE)
+    return TRI_ERR_INVALID_ARG;
   if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
   if (kv->n_layers > 65535 || kv->n_kv_heads > 65536) return TRI_ERR_INVALID_ARG;
   if (!kv->n_valid || !aligned(kv->n_valid, 4) || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
@@ -306,6 +315,7 @@ tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n
   SelectParams p = select_params(nullptr, kv, n_prompt, n_recent, budget, keep_idx);
   p.seed = seed;
   p.round = round;
+  p.draw_scope = scope;
   const cudaError_t e = launch_rand_select(p, static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
@@ -370,7 +380,7 @@ tri_status tri_select_topk_zmax(const float* scores_g, const float* stats, int32
   if (slices_of(kv) > 0x7fffffff) return TRI_ERR_INVALID_ARG;
   const int n_slices = static_cast<int>(slices_of(kv));
   if (final_scores) {
-    const cudaError_t e = launch_zmax_scores(scores_g, stats, kv->n_valid, final_scores, n_slices, kv->n_cap,
+    const cudaError_t e = launch_zmax_scores(scores_g, stats, kv->n_valid, 1, final_scores, n_slices, kv->n_cap,
                                              group, stream);
     if (e != cudaSuccess) return TRI_ERR_CUDA;
   }
@@ -378,6 +388,97 @@ tri_status tri_select_topk_zmax(const float* scores_g, const float* stats, int32
   p.stats = stats;
   p.group = group;
   const cudaError_t e = launch_select_zmax(p, n_slices, stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+namespace {
+// Workspace of tri_select_union: the heads' own picks [S][bk] int32, then
+// stats [S][2] f32, the union bitmaps [groups][words] u32, the member counts
+// [groups] int32 (each part 16-byte aligned).
+struct UnionWs {
+  int32_t bk;
+  int32_t words;
+  size_t keepk_off, stats_off, member_off, count_off, total;
+};
+size_t align16(size_t x) { return (x + 15) / 16 * 16; }
+UnionWs union_ws(const tri_kv* kv, int32_t n_prompt, int32_t n_recent, int32_t k_head) {
+  UnionWs u{};
+  const int64_t S = slices_of(kv);
+  const int64_t groups = S / kv->n_kv_heads;
+  const int64_t bk = (k_head <= 0) ? 0 : std::min<int64_t>(static_cast<int64_t>(n_prompt) + n_recent + k_head,
+                                                           kv->n_cap);
+  u.bk = static_cast<int32_t>(bk);
+  u.words = (kv->n_cap + 31) / 32;
+  u.keepk_off = 0;
+  u.stats_off = align16(u.keepk_off + static_cast<size_t>(S) * bk * sizeof(int32_t));
+  u.member_off = align16(u.stats_off + static_cast<size_t>(S) * 2 * sizeof(float));
+  u.count_off = align16(u.member_off + static_cast<size_t>(groups) * u.words * sizeof(uint32_t));
+  u.total = align16(u.count_off + static_cast<size_t>(groups) * sizeof(int32_t));
+  return u;
+}
+constexpr int32_t UNION_MAX_CAP = 524288;
+}  // namespace
+
+size_t tri_select_union_workspace_bytes(const tri_kv* kv, int32_t n_prompt, int32_t n_recent, int32_t k_head) {
+  if (!kv || kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return 0;
+  if (n_prompt < 0 || n_recent < 0 || k_head < 0) return 0;
+  return union_ws(kv, n_prompt, n_recent, k_head).total;
+}
+
+tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
+                            int32_t budget, int32_t k_head, int32_t* keep_idx, float* final_scores, void* ws,
+                            size_t ws_bytes, tri_stream_t stream) {
+  if (!kv) return TRI_ERR_INVALID_ARG;
+  if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
+  if (kv->n_kv_heads > MAX_GROUP || kv->n_cap > UNION_MAX_CAP) return TRI_ERR_UNSUPPORTED;
+  if (!kv->n_valid || !aligned(kv->n_valid, 4)) return TRI_ERR_INVALID_ARG;
+  if (!scores || !aligned(scores, 4) || !keep_idx || !aligned(keep_idx, 4) || k_head < 0) return TRI_ERR_INVALID_ARG;
+  if (final_scores && !aligned(final_scores, 4)) return TRI_ERR_INVALID_ARG;
+  tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
+  if (slices_of(kv) > 0x7fffffff) return TRI_ERR_INVALID_ARG;
+  const UnionWs u = union_ws(kv, n_prompt, n_recent, k_head);
+  if (!ws || !aligned(ws, 16) || ws_bytes < u.total) return TRI_ERR_INVALID_ARG;
+  const int n_slices = static_cast<int>(slices_of(kv));
+  const int n_groups = n_slices / kv->n_kv_heads;
+  char* base = static_cast<char*>(ws);
+  int32_t* keepk = reinterpret_cast<int32_t*>(base + u.keepk_off);
+  float* stats = reinterpret_cast<float*>(base + u.stats_off);
+  uint32_t* member = reinterpret_cast<uint32_t*>(base + u.member_off);
+  int32_t* ucount = reinterpret_cast<int32_t*>(base + u.count_off);
+  cudaError_t e;
+  if (u.bk > 0) {  // 1. every head's own picks
+    e = launch_select(select_params(scores, kv, n_prompt, n_recent, u.bk, keepk), n_slices, stream);
+    if (e != cudaSuccess) return TRI_ERR_CUDA;
+  }
+  UnionPrepParams q{};  // 2. statistics and the union
+  q.scores = scores;
+  q.n_valid = kv->n_valid;
+  q.keepk = keepk;
+  q.stats = stats;
+  q.member = member;
+  q.ucount = ucount;
+  q.dev_status = kv->dev_status;
+  q.n_cap = kv->n_cap;
+  q.bk = u.bk;
+  q.n_prompt = n_prompt;
+  q.n_recent = n_recent;
+  q.group = kv->n_kv_heads;
+  q.member_words = u.words;
+  e = launch_union_prep(q, n_groups, stream);
+  if (e != cudaSuccess) return TRI_ERR_CUDA;
+  if (final_scores) {
+    e = launch_zmax_scores(scores, stats, kv->n_valid, kv->n_kv_heads, final_scores, n_groups, kv->n_cap,
+                           kv->n_kv_heads, stream);
+    if (e != cudaSuccess) return TRI_ERR_CUDA;
+  }
+  SelectParams p = select_params(scores, kv, n_prompt, n_recent, budget, keep_idx);  // 3. one list per group
+  p.stats = stats;
+  p.group = kv->n_kv_heads;
+  p.member = member;
+  p.ucount = ucount;
+  p.member_words = u.words;
+  e = launch_select_union(p, n_groups, stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 

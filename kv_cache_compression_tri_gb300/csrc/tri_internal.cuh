@@ -223,9 +223,25 @@ struct SelectParams {
   int32_t n_layers, n_kv_heads;
   uint64_t seed;
   uint32_t round;
+  int32_t draw_scope;  // 0: a draw per KV head; 1: one per (seq, layer); 2: one per sequence
   // z-score + max source: per-head scores [S][group][n_cap], stats [S][group][2]
   const float* stats;
   int32_t group;
+  // union source: per-group union bitmap [groups][member_words], member counts [groups]
+  const uint32_t* member;
+  const int32_t* ucount;
+  int32_t member_words;
+};
+
+struct UnionPrepParams {
+  const float* scores;    // [S][n_cap], every valid row scored
+  const int32_t* n_valid;
+  const int32_t* keepk;   // [S][bk]: each slice's own top picks (or NULL when bk == 0)
+  float* stats;           // [S][2] out: mean, std over rows [0, n_valid)
+  uint32_t* member;       // [groups][member_words] out
+  int32_t* ucount;        // [groups] out
+  int32_t* dev_status;
+  int32_t n_cap, bk, n_prompt, n_recent, group, member_words;
 };
 
 struct CompactParams {
@@ -277,8 +293,12 @@ cudaError_t launch_score_heads(const ScoreParams& p, int n_heads, tri_dtype dt, 
                                tri_rope_style style, int pos_mode, int n_slices, cudaStream_t st);
 cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slices, int tiles_per_slice,
                                int group, cudaStream_t st);
-cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid,
-                               float* out, int n_slices, int n_cap, int group, cudaStream_t st);
+// out[b][i] = max_g z of rows [b*group, b*group+group) for blocks b < n_blocks;
+// the valid row count of block b is n_valid[b * nv_stride].
+cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid, int nv_stride,
+                               float* out, int n_blocks, int n_cap, int group, cudaStream_t st);
+cudaError_t launch_union_prep(const UnionPrepParams& q, int n_groups, cudaStream_t st);
+cudaError_t launch_select_union(const SelectParams& p, int n_groups, cudaStream_t st);
 cudaError_t launch_select_zmax(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st);

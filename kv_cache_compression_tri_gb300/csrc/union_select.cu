@@ -1,0 +1,129 @@
+// union_select.cu -- the group pass of union-based selection across heads.
+//
+// TriAttention blog, "eviction (union-based selection)": the KV heads that
+// share one keep list (here the H KV heads of one (seq, layer)) each pick
+// their own top candidates; the union of the picks is kept first, ranked by a
+// combined score, and topped up by the combined score when it is smaller
+// than the budget. The picks come from the ordinary per-slice selection
+// (select.cu, budget P + W + k_head); the final ranking is the grouped key
+// source of select.cu. Between them this kernel, one CTA per group:
+//   * the mean and standard deviation of each slice's scores over its valid
+//     rows (two passes over the slice: the mean, then the centred squares),
+//     which turn the scores into the z-scores of the combined score
+//     max_h z_h (TriAttention paper summary, "Handling Grouped-Query
+//     Attention": normalise, then take the maximum);
+//   * the union of the heads' picks as a bitmap over the slots, and its size.
+// The heads of a group must hold the same number of rows (their keep list is
+// shared); a group that does not sets TRI_DEV_GROUP_NVALID and keeps nothing
+// from the union.
+#include <cuda_runtime.h>
+
+#include <math.h>
+
+#include "tri_internal.cuh"
+
+namespace tri {
+namespace {
+
+constexpr int UT = 256;
+constexpr int UW = UT / 32;
+
+// Sum over the CTA in fp64, fixed order (lanes, then warps); every thread
+// gets the result.
+__device__ __forceinline__ double block_sum(double v, double* sred) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(FULL_MASK, v, o);
+  if (lane == 0) sred[w] = v;
+  __syncthreads();
+  double tot = 0.0;
+#pragma unroll
+  for (int j = 0; j < UW; ++j) tot += sred[j];
+  __syncthreads();  // sred is reused by the next call
+  return tot;
+}
+
+__global__ void __launch_bounds__(UT) union_prep_kernel(const __grid_constant__ UnionPrepParams q) {
+  extern __shared__ __align__(16) uint32_t sbits[];  // [member_words]
+  __shared__ double sred[UW];
+  __shared__ int sbad;
+  const int t = threadIdx.x;
+  const int64_t g = blockIdx.x;
+  const int64_t s0 = g * q.group;
+  uint32_t* member = q.member + g * q.member_words;
+
+  if (t == 0) sbad = 0;
+  __syncthreads();
+  const int n = q.n_valid[s0];
+  if (t < q.group && q.n_valid[s0 + t] != n) atomicExch(&sbad, 1);
+  for (int j = t; j < q.member_words; j += UT) sbits[j] = 0u;
+  __syncthreads();
+  if (sbad || n < 0 || n > q.n_cap) {
+    if (t == 0) {
+      if (sbad) set_status(q.dev_status, TRI_DEV_GROUP_NVALID);
+      q.ucount[g] = 0;
+    }
+    for (int j = t; j < q.member_words; j += UT) member[j] = 0u;
+    for (int h = t; h < q.group; h += UT) {
+      q.stats[(s0 + h) * 2] = 0.f;
+      q.stats[(s0 + h) * 2 + 1] = 0.f;
+    }
+    return;
+  }
+
+  // ---- statistics of every slice of the group ------------------------------
+  for (int h = 0; h < q.group; ++h) {
+    const float* row = q.scores + (s0 + h) * static_cast<int64_t>(q.n_cap);
+    float a = 0.f;
+    for (int i = t; i < n; i += UT) a += __ldcg(row + i);
+    const double mean = (n > 0) ? block_sum(a, sred) / n : 0.0;
+    const float mf = static_cast<float>(mean);
+    float b = 0.f;
+    for (int i = t; i < n; i += UT) {
+      const float d = __ldcg(row + i) - mf;
+      b = fmaf(d, d, b);
+    }
+    // the centred sum uses the fp32 mean; correct it to the fp64 one
+    const double dm = mean - static_cast<double>(mf);
+    const double ss = block_sum(b, sred);
+    const double var = (n > 0) ? fmax(ss / n - dm * dm, 0.0) : 0.0;
+    if (t == 0) {
+      q.stats[(s0 + h) * 2] = mf;
+      q.stats[(s0 + h) * 2 + 1] = static_cast<float>(sqrt(var));
+    }
+  }
+
+  // ---- the union of the heads' own picks ----------------------------------
+  // The picks are the candidates [P, n - W) in each slice's keep list.
+  const int lo = q.n_prompt, hi = n - q.n_recent;
+  for (int h = 0; h < q.group && q.bk > 0; ++h) {
+    const int32_t* kk = q.keepk + (s0 + h) * static_cast<int64_t>(q.bk);
+    for (int j = t; j < q.bk; j += UT) {
+      const int v = __ldg(kk + j);
+      if (v >= lo && v < hi) atomicOr(&sbits[v >> 5], 1u << (v & 31));
+    }
+  }
+  __syncthreads();
+  int cnt = 0;
+  for (int j = t; j < q.member_words; j += UT) {
+    const uint32_t w = sbits[j];
+    member[j] = w;
+    cnt += __popc(w);
+  }
+  const double tot = block_sum(static_cast<double>(cnt), sred);
+  if (t == 0) q.ucount[g] = static_cast<int32_t>(tot);
+}
+
+}  // namespace
+
+cudaError_t launch_union_prep(const UnionPrepParams& q, int n_groups, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(q.member_words) * sizeof(uint32_t);
+  const cudaError_t e = cudaFuncSetAttribute(union_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  union_prep_kernel<<<static_cast<unsigned>(n_groups), UT, smem, st>>>(q);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace tri

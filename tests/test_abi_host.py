@@ -99,6 +99,7 @@ def test_select_rejects_bad_budget(lib):
     assert lib.tri_select_topk(0x60000, None, 0, 0, 64, 0x50000, None) == INVALID
     assert lib.rand_evict(ctypes.byref(kv), 0, 0, 40, 40, 64, 0x50000, None) == INVALID
     assert lib.rand_evict(ctypes.byref(_kv(n_layers=70000)), 0, 0, 0, 0, 64, 0x50000, None) == INVALID
+    assert lib.rand_evict_scoped(ctypes.byref(kv), 0, 0, 3, 0, 0, 64, 0x50000, None) == INVALID  # no such scope
 
 
 def test_score_rejects_bad_args(lib):

@@ -308,6 +308,34 @@ def test_random_bit_exact(P, W):
             assert np.array_equal(g[s], exp), (rnd, s)
 
 
+@pytest.mark.parametrize("scope", [1, 2])
+def test_random_shared_draw(scope):
+    # Random Attention's shared-draw control: one keep-set for every head of a
+    # layer (scope 1) or of a sequence (scope 2)
+    w = synth.scaled(LAYER, n_seq=2, n_layers=3, n_kv_heads=4, n_cap=6000, n_valid=6000)
+    S = w.n_slices
+    k = torch.zeros(w.n_seq, w.n_layers, w.n_kv_heads, 6000, 64, dtype=torch.bfloat16, device="cuda")
+    kv = tri.KVCache(k, k, torch.full((S,), 6000, dtype=torch.int32, device="cuda"), None, None,
+                     torch.zeros(1, dtype=torch.int32, device="cuda"))
+    B, P = 1500, 100
+    keep = torch.full((S, B), -9, dtype=torch.int32, device="cuda")
+    tri.rand_evict_scoped(kv, 0xABCDEF, 5, scope, P, 0, B, keep)
+    torch.cuda.synchronize()
+    g = keep.cpu().numpy()
+    for s in range(S):
+        seq, rem = divmod(s, w.n_layers * w.n_kv_heads)
+        layer, head = divmod(rem, w.n_kv_heads)
+        exp = orc.rand_select_shared(0xABCDEF, 5, seq, layer, head, scope, 6000, P, 0, B)
+        assert np.array_equal(g[s], exp), s
+        first = seq * w.n_layers * w.n_kv_heads + (0 if scope == 2 else layer * w.n_kv_heads)
+        assert np.array_equal(g[s], g[first])
+    # per-head draws differ from head to head
+    tri.rand_evict_scoped(kv, 0xABCDEF, 5, 0, P, 0, B, keep)
+    torch.cuda.synchronize()
+    g0 = keep.cpu().numpy()
+    assert not np.array_equal(g0[0], g0[1])
+
+
 def test_nvalid_over_capacity_sets_status():
     w = synth.scaled(TINY, n_kv_heads=2, n_cap=256, n_valid=256, dtype=torch.bfloat16)
     inp = synth.make_inputs(w, "cuda")

@@ -1,0 +1,96 @@
+"""GPU parity of union-based selection across the KV heads of a (seq, layer)
+(TriAttention blog, "eviction (union-based selection)") through the C ABI.
+
+The selection is decided in fp32 on the GPU, so it is checked against the
+oracle's two steps run on the GPU's own fp32 inputs: the union of every
+head's top k_head picks (from the GPU's fp32 scores: exact, integer work) and
+the final ranking of the GPU's fp32 combined scores (bit for bit). The
+combined scores themselves are checked against the fp64 oracle's z-score
+maximum of the same fp32 scores within fp32 rounding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import kv_cache_compression_tri_gb300 as tri
+from kv_cache_compression_tri_gb300 import synth
+from gpu_helpers import make_cache
+
+pytestmark = pytest.mark.gpu
+
+LAYER = synth.WORKLOADS["qwen3_8b_layer"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    tri.load_library()
+
+
+def _union_case(w, P, W, B, k_head, nv=None, seed=0):
+    inp = synth.make_inputs(w, "cuda")
+    S, n_cap, H = w.n_slices, w.n_cap, w.n_kv_heads
+    if nv is not None:
+        inp.n_valid = torch.tensor(nv, dtype=torch.int32, device="cuda")
+    c = tri.calibrate_centers(inp.q, w.group)
+    kv = make_cache(inp)
+    scores = torch.zeros(S, n_cap, device="cuda")
+    tri.score(kv, c, w.theta, w.offsets, inp.p_cur, scores)  # every valid row
+    keep = torch.full((S, B), -9, dtype=torch.int32, device="cuda")
+    groups = S // H
+    final = torch.full((groups, n_cap), 777.0, device="cuda")
+    n0 = tri.launch_count()
+    tri.select_union(scores, kv, P, W, B, k_head, keep, final_scores=final)
+    assert tri.launch_count() - n0 == (4 if k_head > 0 else 3)
+    torch.cuda.synchronize()
+    assert int(kv.dev_status.item()) == 0
+    g_sc, g_keep, g_fin = scores.cpu().numpy(), keep.cpu().numpy(), final.cpu().numpy()
+    nvh = kv.n_valid.cpu().numpy()
+    for g in range(groups):
+        rows = slice(g * H, (g + 1) * H)
+        n = int(nvh[g * H])
+        for h in range(1, H):
+            assert np.array_equal(g_keep[g * H + h], g_keep[g * H]), (g, h)
+        s64 = g_sc[rows, :n].astype(np.float64)
+        mu, sd, comb = orc.zscore_max(s64)
+        tol = 1e-5 * (1.0 + np.abs(comb) + np.max(np.abs(mu) / np.where(sd > 0, sd, 1.0)))
+        assert np.all(np.abs(g_fin[g, :n] - comb) <= tol), g
+        assert np.all(g_fin[g, n:] == 777.0)
+        if n <= B:
+            assert g_keep[g * H].tolist() == list(range(n)) + [-1] * (B - n)
+            continue
+        member = orc.union_members(s64, P, W, k_head)
+        exp = orc.union_rank(member, g_fin[g, :n].astype(np.float64), P, W, B)
+        assert np.array_equal(g_keep[g * H], exp), g
+        # and the whole oracle on the same fp32 scores agrees away from near ties
+        keep_ref, member_ref, _ = orc.union_select(s64, n, P, W, B, k_head)
+        assert np.array_equal(member_ref, member)
+        assert len(set(keep_ref.tolist()) ^ set(exp.tolist())) <= 2 * max(1, B // 200)
+
+
+@pytest.mark.parametrize("k_head", [0, 40, 300, 1664, 5000])
+def test_union_layer_workload(k_head):
+    # 8 KV heads share one list; need = 2048 - 256 - 128 = 1664
+    w = synth.scaled(LAYER, n_seq=2, n_layers=2)
+    _union_case(w, 256, 128, 2048, k_head)
+
+
+def test_union_small_groups_and_ragged_groups():
+    w = synth.scaled(LAYER, n_seq=2, n_layers=3, n_kv_heads=3, group=2, n_cap=5000, n_valid=5000, n_cal=512)
+    nv = np.repeat([5000, 4001, 2500, 300, 4999, 1200], 3)  # equal within each (seq, layer)
+    _union_case(w, 17, 33, 1000, 100, nv=nv)
+    _union_case(w, 0, 0, 700, 5, nv=nv)
+
+
+def test_union_mismatched_group_sets_status():
+    w = synth.scaled(LAYER, n_kv_heads=2, n_cap=600, n_valid=600, n_cal=256)
+    inp = synth.make_inputs(w, "cuda", with_queries=False)
+    kv = make_cache(inp)
+    kv.n_valid[1] = 599
+    scores = torch.randn(w.n_slices, 600, device="cuda")
+    keep = torch.empty(w.n_slices, 100, dtype=torch.int32, device="cuda")
+    tri.select_union(scores, kv, 0, 0, 100, 10, keep)
+    torch.cuda.synchronize()
+    assert int(kv.dev_status.item()) == tri.DEV_GROUP_NVALID
