@@ -63,6 +63,7 @@ typedef enum {
 #define TRI_DEV_BAD_KEEP 3        /* keep list not ascending / out of range       */
 #define TRI_DEV_TIMEOUT 4         /* a bounded in-kernel wait gave up (~2 s)      */
 #define TRI_DEV_GROUP_NVALID 5    /* slices sharing a keep list differ in n_valid */
+#define TRI_DEV_BAD_BLOCK 6       /* a block table entry is outside [0, num_blocks) */
 
 typedef enum { TRI_F32 = 0, TRI_BF16 = 1 } tri_dtype;
 
@@ -106,6 +107,20 @@ typedef struct {
   tri_dtype dtype;       /* element type of k and v                              */
   int32_t* dev_status;   /* device int32 status word (TRI_DEV_*), or NULL        */
   tri_key_layout key_layout; /* pre- or post-RoPE keys (0 = pre-RoPE)            */
+  /* Paged caches (block_table != NULL; [RA] section 6: the score is a pass
+   * "through vLLM's block tables", eviction rewrites the survivors into the
+   * request's blocks and frees the tail). k and v are then block pools, and
+   * logical row r of slice (seq, layer, head) is at element
+   *   block_table[seq][r / block_size] * block_stride + layer * layer_stride
+   *   + head * head_stride + (r % block_size) * head_dim
+   * of k (and of v): every (block, layer, head) holds block_size contiguous
+   * rows. One table per sequence, shared by its layers and heads; n_cap =
+   * (table entries per sequence) * block_size; slice_stride is ignored. All
+   * fields below are ignored when block_table is NULL. */
+  const int32_t* block_table; /* device [n_seq][n_cap / block_size], or NULL    */
+  int32_t block_size;         /* rows per block, a multiple of 16                */
+  int32_t num_blocks;         /* blocks per pool; every used entry must be below  */
+  int64_t block_stride, layer_stride, head_stride; /* elements; x elem size % 16 == 0 */
 } tri_kv;
 
 /* Per-(layer, KV head) query statistics, [TA] "Offline Calibration
@@ -118,7 +133,7 @@ typedef struct {
 
 /* ------------------------------------------------------------------------ */
 const char* tri_status_string(tri_status s); /* static text, never NULL */
-int32_t tri_abi_version(void);               /* 2 */
+int32_t tri_abi_version(void);               /* 3 */
 /* Kernels this library has launched in this process (all devices, all
  * threads); used to count launches inside a timed region. */
 uint64_t tri_launch_count(void);
@@ -339,6 +354,15 @@ size_t tri_select_union_workspace_bytes(const tri_kv* kv, int32_t n_prompt, int3
 tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
                             int32_t budget, int32_t k_head, int32_t* keep_idx, float* final_scores, void* ws,
                             size_t ws_bytes, tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tri_paged_blocks_used -- after a compaction of a paged cache: the blocks
+ * each sequence still uses, ceil(max over its slices of n_valid / block_size);
+ * table entries from there on hold no live row and can go back to the
+ * caller's allocator ([RA] section 6: "free the tail"). blocks_used: device
+ * [n_seq] int32. Requires a paged cache (block_table != NULL).
+ * ------------------------------------------------------------------------ */
+tri_status tri_paged_blocks_used(const tri_kv* kv, int32_t* blocks_used, tri_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "TriError", "KVCache", "Centers", "lib_path", "load_library", "calibrate_centers",
+    "TriError", "KVCache", "PagedKVCache", "paged_blocks_used", "Centers", "lib_path", "load_library", "calibrate_centers",
     "calibrate_workspace_bytes", "score", "select_topk", "compact_kv", "rand_evict",
     "compress", "compress_workspace_bytes", "score_heads", "score_heads_workspace_bytes",
     "select_topk_zmax", "select_union", "select_union_workspace_bytes", "rand_evict_scoped", "DRAW_PER_HEAD", "DRAW_PER_LAYER", "DRAW_PER_SEQUENCE",
@@ -30,7 +30,8 @@ __all__ = [
 ROPE_INTERLEAVED, ROPE_HALF = 0, 1
 NORM_WEIGHTED, NORM_UNWEIGHTED = 0, 1
 F32, BF16 = 0, 1
-DEV_OK, DEV_NVALID_OVER_CAP, DEV_NAN_SCORE, DEV_BAD_KEEP, DEV_TIMEOUT, DEV_GROUP_NVALID = 0, 1, 2, 3, 4, 5
+DEV_OK, DEV_NVALID_OVER_CAP, DEV_NAN_SCORE, DEV_BAD_KEEP, DEV_TIMEOUT, DEV_GROUP_NVALID, DEV_BAD_BLOCK = (
+    0, 1, 2, 3, 4, 5, 6)
 
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -49,6 +50,8 @@ class _TriKV(ctypes.Structure):
         ("n_layers", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
         ("n_cap", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int),
         ("dev_status", ctypes.c_void_p), ("key_layout", ctypes.c_int),
+        ("block_table", ctypes.c_void_p), ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+        ("block_stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64),
     ]
 
 
@@ -113,6 +116,8 @@ def load_library():
         lib.tri_select_union_workspace_bytes.restype = ctypes.c_size_t
         lib.tri_select_union.argtypes = [vp, kvp, i32, i32, i32, i32, vp, vp, vp, ctypes.c_size_t, vp]
         lib.tri_select_union.restype = ctypes.c_int
+        lib.tri_paged_blocks_used.argtypes = [kvp, vp, vp]
+        lib.tri_paged_blocks_used.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -176,6 +181,14 @@ class KVCache:
         s = self.k.shape
         return s[0] * s[1] * s[2]
 
+    @property
+    def n_cap(self) -> int:
+        return self.k.shape[3]
+
+    @property
+    def device(self):
+        return self.k.device
+
     def _abi(self) -> _TriKV:
         n_seq, L, H, n_cap, d = self.k.shape
         assert self.k.is_cuda and self.k.dtype in _DTYPES
@@ -191,7 +204,68 @@ class KVCache:
                 assert t.dtype == torch.int32 and t.is_contiguous() and t.numel() == n_seq * L * H * n_cap
         return _TriKV(self.k.data_ptr(), self.v.data_ptr(), _ptr(self.pos), _ptr(self.pos_out),
                       self.n_valid.data_ptr(), stride, n_seq, L, H, n_cap, d, _DTYPES[self.k.dtype],
-                      _ptr(self.dev_status), 1 if self.post_rope else 0)
+                      _ptr(self.dev_status), 1 if self.post_rope else 0, None, 0, 0, 0, 0, 0)
+
+
+@dataclass
+class PagedKVCache:
+    """A paged batch of caches: k, v pools [num_blocks, n_layers, n_kv_heads,
+    block_size, head_dim] (bf16 or fp32, device; any strides that keep each
+    (block, layer, head) run of block_size rows contiguous); block_table
+    [n_seq, blocks per sequence] int32 (physical block of each logical block,
+    shared by the sequence's layers and heads); n_valid [S] int32; pos /
+    pos_out [S, n_cap] int32 with n_cap = blocks per sequence * block_size."""
+    k: torch.Tensor
+    v: torch.Tensor
+    block_table: torch.Tensor
+    n_valid: torch.Tensor
+    pos: torch.Tensor | None
+    pos_out: torch.Tensor | None
+    dev_status: torch.Tensor | None = None
+    post_rope: bool = False
+
+    @property
+    def n_seq(self) -> int:
+        return self.block_table.shape[0]
+
+    @property
+    def n_slices(self) -> int:
+        return self.n_seq * self.k.shape[1] * self.k.shape[2]
+
+    @property
+    def n_cap(self) -> int:
+        return self.block_table.shape[1] * self.k.shape[3]
+
+    @property
+    def device(self):
+        return self.k.device
+
+    def _abi(self) -> _TriKV:
+        nb, L, H, bs, d = self.k.shape
+        assert self.k.is_cuda and self.k.dtype in _DTYPES
+        assert self.v.shape == self.k.shape and self.v.dtype == self.k.dtype
+        assert tuple(self.v.stride()) == tuple(self.k.stride())
+        assert self.k.stride(4) == 1 and self.k.stride(3) == d
+        assert self.block_table.dtype == torch.int32 and self.block_table.is_contiguous()
+        S, n_cap = self.n_slices, self.n_cap
+        assert self.n_valid.dtype == torch.int32 and self.n_valid.numel() == S
+        for t in (self.pos, self.pos_out):
+            if t is not None:
+                assert t.dtype == torch.int32 and t.is_contiguous() and t.numel() == S * n_cap
+        return _TriKV(self.k.data_ptr(), self.v.data_ptr(), _ptr(self.pos), _ptr(self.pos_out),
+                      self.n_valid.data_ptr(), 0, self.n_seq, L, H, n_cap, d, _DTYPES[self.k.dtype],
+                      _ptr(self.dev_status), 1 if self.post_rope else 0, self.block_table.data_ptr(), bs, nb,
+                      self.k.stride(0), self.k.stride(1), self.k.stride(2))
+
+
+def paged_blocks_used(kv: PagedKVCache, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Blocks each sequence still uses after compaction (tri_paged_blocks_used);
+    table entries from there on are free. out: [n_seq] int32."""
+    lib = load_library()
+    assert out.dtype == torch.int32 and out.is_contiguous() and out.numel() == kv.n_seq
+    kvs = kv._abi()
+    _check("tri_paged_blocks_used", lib.tri_paged_blocks_used(ctypes.byref(kvs), out.data_ptr(), _stream(stream)))
+    return out
 
 
 def calibrate_workspace_bytes(n_layers: int, n_q_heads: int, group: int, head_dim: int,
@@ -230,7 +304,7 @@ def score(kv: KVCache, centers: Centers, rope_theta: float, offsets, p_cur: torc
     offs = (ctypes.c_int32 * len(offsets))(*[int(o) for o in offsets])
     assert p_cur.dtype == torch.int64 and p_cur.is_cuda
     assert scores.dtype == torch.float32 and scores.is_contiguous()
-    assert scores.numel() == kv.n_slices * kv.k.shape[3]
+    assert scores.numel() == kv.n_slices * kv.n_cap
     kvs, cs = kv._abi(), centers._abi()
     _check("tri_score", lib.tri_score(ctypes.byref(kvs), ctypes.byref(cs), float(rope_theta), style,
                                       norm_mode, ctypes.cast(offs, ctypes.c_void_p), len(offsets),
@@ -302,7 +376,7 @@ def compress(kv: KVCache, centers: Centers, rope_theta: float, offsets, p_cur: t
     kvs, cs = kv._abi(), centers._abi()
     need = int(lib.tri_compress_workspace_bytes(ctypes.byref(kvs)))
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=kv.k.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=kv.device)
     assert workspace.numel() >= need
     _check("tri_compress", lib.tri_compress(ctypes.byref(kvs), ctypes.byref(cs), float(rope_theta), style,
                                             norm_mode, ctypes.cast(offs, ctypes.c_void_p), len(offsets),
@@ -326,12 +400,12 @@ def score_heads(kv: KVCache, centers: Centers, group: int, rope_theta: float, of
     offs = (ctypes.c_int32 * len(offsets))(*[int(o) for o in offsets])
     assert p_cur.dtype == torch.int64 and p_cur.is_cuda
     assert scores_g.dtype == torch.float32 and scores_g.is_contiguous()
-    assert scores_g.numel() == kv.n_slices * group * kv.k.shape[3]
+    assert scores_g.numel() == kv.n_slices * group * kv.n_cap
     assert stats.dtype == torch.float32 and stats.is_contiguous() and stats.numel() == kv.n_slices * group * 2
     kvs, cs = kv._abi(), centers._abi()
     need = int(lib.tri_score_heads_workspace_bytes(ctypes.byref(kvs), group))
     if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=kv.k.device)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=kv.device)
     assert workspace.numel() >= need
     _check("tri_score_heads", lib.tri_score_heads(
         ctypes.byref(kvs), ctypes.byref(cs), group, float(rope_theta), style, norm_mode,
@@ -349,7 +423,7 @@ def select_topk_zmax(scores_g: torch.Tensor, stats: torch.Tensor, group: int, kv
     assert keep.dtype == torch.int32 and keep.is_contiguous() and keep.numel() == kv.n_slices * budget
     if final_scores is not None:
         assert final_scores.dtype == torch.float32 and final_scores.is_contiguous()
-        assert final_scores.numel() == kv.n_slices * kv.k.shape[3]
+        assert final_scores.numel() == kv.n_slices * kv.n_cap
     kvs = kv._abi()
     _check("tri_select_topk_zmax", lib.tri_select_topk_zmax(
         scores_g.data_ptr(), stats.data_ptr(), group, ctypes.byref(kvs), n_prompt, n_recent, budget,
@@ -373,7 +447,7 @@ def select_union(scores: torch.Tensor, kv: KVCache, n_prompt: int, n_recent: int
     kvs = kv._abi()
     need = int(lib.tri_select_union_workspace_bytes(ctypes.byref(kvs), n_prompt, n_recent, k_head))
     if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=kv.k.device)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=kv.device)
     assert workspace.numel() >= need
     if final_scores is not None:
         assert final_scores.dtype == torch.float32 and final_scores.is_contiguous()

@@ -20,7 +20,10 @@
 //     safe: every source of a later tile is >= (u+1)*TR, above every row tile
 //     u writes, and tile u's own sources were read before its store was
 //     issued.
-// Waits on gathers are bounded in wall-clock time (TRI_DEV_TIMEOUT).
+// A paged cache (block table per sequence) moves the same logical rows; the
+// physical rows come from the table, and a tile's store is split where its
+// destinations cross a block boundary. Waits on gathers are bounded in
+// wall-clock time (TRI_DEV_TIMEOUT).
 #include <cuda_runtime.h>
 
 #include "tri_internal.cuh"
@@ -37,8 +40,10 @@ constexpr int POS_PER_THREAD = 8;
 
 // Rows [first, n_keep) of one tensor of one slice, moved by one warp
 // through a ring of CSTAGES tiles of CTILE bytes (see the file comment).
-__device__ __forceinline__ void move_rows(char* base, unsigned char* ring, uint64_t* full, const int32_t* keep,
-                                          int first, int n_keep, int rb, int lane, int32_t* dev_status) {
+// Row r of the slice is at pool + rows.row(sbase, trow, r).
+__device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_t sbase, const int32_t* trow,
+                                          unsigned char* ring, uint64_t* full, const int32_t* keep, int first,
+                                          int n_keep, int rb, int lane, int32_t* dev_status) {
   const int TR = CTILE / rb;  // rows per tile
   const int u_first = first / TR;
   const int ntiles = (n_keep - 1) / TR - u_first + 1;
@@ -54,20 +59,21 @@ __device__ __forceinline__ void move_rows(char* base, unsigned char* ring, uint6
     lo_j = max(t0, first);
     hi_j = min(t0 + TR, n_keep);
   };
-  // Each lane copies rows lo_j + lane + 32 r of a tile (r < RPL); their keep
-  // entries are loaded one tile ahead so no gather waits on them.
+  // Each lane copies rows lo_j + lane + 32 r of a tile (r < RPL); the byte
+  // offsets of their sources (keep entry, and block for a paged cache) are
+  // resolved one tile ahead so no gather waits on them.
   constexpr int RPL = CTILE / 128 / 32;  // most rows a lane copies per tile (2)
-  int knext[RPL];
-  auto load_keep = [&](int k, int (&kv)[RPL]) {
+  int64_t knext[RPL];
+  auto load_keep = [&](int k, int64_t (&kv)[RPL]) {
     int lo_j, hi_j, t0;
     rows_of(k, lo_j, hi_j, t0);
 #pragma unroll
     for (int r = 0; r < RPL; ++r) {
       const int j = lo_j + lane + 32 * r;
-      kv[r] = (k < ntiles && j < hi_j) ? __ldg(keep + j) : 0;
+      kv[r] = (k < ntiles && j < hi_j) ? rows.row(sbase, trow, __ldg(keep + j)) : 0;
     }
   };
-  auto gather = [&](int k, const int (&kv)[RPL]) {
+  auto gather = [&](int k, const int64_t (&kv)[RPL]) {
     int lo_j, hi_j, t0;
     rows_of(k, lo_j, hi_j, t0);
     const int st = k % CSTAGES;
@@ -76,14 +82,12 @@ __device__ __forceinline__ void move_rows(char* base, unsigned char* ring, uint6
 #pragma unroll
     for (int r = 0; r < RPL; ++r) {
       const int j = lo_j + lane + 32 * r;
-      if (j < hi_j)
-        bulk_g2s(ring + st * CTILE + (j - t0) * rb, base + static_cast<int64_t>(kv[r]) * rb,
-                 static_cast<uint32_t>(rb), &full[st]);
+      if (j < hi_j) bulk_g2s(ring + st * CTILE + (j - t0) * rb, pool + kv[r], static_cast<uint32_t>(rb), &full[st]);
     }
   };
 
   for (int k = 0; k < min(CSTAGES - 1, ntiles); ++k) {
-    int kv[RPL];
+    int64_t kv[RPL];
     load_keep(k, kv);
     gather(k, kv);
   }
@@ -96,15 +100,20 @@ __device__ __forceinline__ void move_rows(char* base, unsigned char* ring, uint6
     ok = __all_sync(FULL_MASK, ok);
     if (!ok) break;
     if (lane == 0) {
+      // the tile's destinations are consecutive rows: one store per run of
+      // them that is contiguous in memory (all of them, or per block)
       int lo_j, hi_j, t0;
       rows_of(k, lo_j, hi_j, t0);
-      bulk_s2g(base + static_cast<int64_t>(lo_j) * rb, ring + st * CTILE + (lo_j - t0) * rb,
-               static_cast<uint32_t>((hi_j - lo_j) * rb));
+      for (int j = lo_j; j < hi_j;) {
+        const int run = rows.run(j, hi_j - j);
+        bulk_s2g(pool + rows.row(sbase, trow, j), ring + st * CTILE + (j - t0) * rb, static_cast<uint32_t>(run * rb));
+        j += run;
+      }
       bulk_commit();
     }
     const int kn = k + CSTAGES - 1;  // refills the stage of tile k - 1
     if (kn < ntiles) {
-      int kv[RPL];
+      int64_t kv[RPL];
 #pragma unroll
       for (int r = 0; r < RPL; ++r) kv[r] = knext[r];
       load_keep(kn + 1, knext);
@@ -127,6 +136,8 @@ struct CSmem {
   int bad;
   int n_keep;
   int first_move;
+  int last_src;
+  int bad_block;
 };
 
 __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ CompactParams p) {
@@ -140,13 +151,14 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
     sm.bad = 0;
     sm.n_keep = p.budget;
     sm.first_move = p.budget;
+    sm.last_src = -1;
   }
   __syncthreads();
   // Validate the keep list before touching anything: ascending, keep[j] >= j,
   // < n_cap, and -1 only as trailing padding. Each thread checks runs of 4
   // entries (one 16-byte load when the list is 16-byte aligned).
   const bool vec = (p.budget % 4 == 0) && ((reinterpret_cast<uintptr_t>(keep) & 15) == 0);
-  int bad = 0, nk = p.budget, fm = p.budget;
+  int bad = 0, nk = p.budget, fm = p.budget, ls = -1;
   for (int j0 = 4 * t; j0 < p.budget; j0 += 4 * CT) {
     int v[4];
     if (vec) {
@@ -168,6 +180,7 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
       } else {
         bad |= (kj < j || kj >= p.n_cap || (j > 0 && (prev < 0 || prev >= kj)));
         if (kj != j) fm = min(fm, j);
+        ls = max(ls, kj);
       }
       prev = kj;
     }
@@ -177,11 +190,13 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
     bad |= __shfl_xor_sync(FULL_MASK, bad, o);
     nk = min(nk, __shfl_xor_sync(FULL_MASK, nk, o));
     fm = min(fm, __shfl_xor_sync(FULL_MASK, fm, o));
+    ls = max(ls, __shfl_xor_sync(FULL_MASK, ls, o));
   }
   if (lane == 0) {
     if (bad) atomicOr(&sm.bad, 1);
     atomicMin(&sm.n_keep, nk);
     atomicMin(&sm.first_move, fm);
+    atomicMax(&sm.last_src, ls);
   }
   __syncthreads();
   if (sm.bad) {
@@ -190,12 +205,19 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   }
   const int n_keep = sm.n_keep;
   const int first = min(sm.first_move, n_keep);
+  // a paged cache: every block the move reads or writes must be in the pool
+  const int64_t sbase = p.rows.slice_base(s);
+  const int32_t* trow = p.rows.seq_table(s);
+  if (!p.rows.blocks_ok(trow, 0, max(sm.last_src + 1, n_keep), &sm.bad_block)) {
+    if (t == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
+    return;
+  }
 
   const int wid = t >> 5;
   if (wid < 2) {
     // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
     if (first < n_keep)
-      move_rows((wid == 0 ? p.k : p.v) + s * p.slice_bytes, smem + wid * RING_BYTES,
+      move_rows(wid == 0 ? p.k : p.v, p.rows, sbase, trow, smem + wid * RING_BYTES,
                 reinterpret_cast<uint64_t*>(smem + 2 * RING_BYTES) + wid * CSTAGES, keep, first, n_keep,
                 p.row_bytes, lane, p.dev_status);
     return;
@@ -230,7 +252,23 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   if (pt == 0) p.n_valid[s] = n_keep;
 }
 
+// One thread per sequence: blocks still holding live rows after compaction.
+__global__ void blocks_used_kernel(const RowMap rows, const int32_t* __restrict__ n_valid, int32_t* out, int n_seq) {
+  const int seq = blockIdx.x * blockDim.x + threadIdx.x;
+  if (seq >= n_seq) return;
+  int most = 0;
+  for (int j = 0; j < rows.lh_count; ++j) most = max(most, n_valid[static_cast<int64_t>(seq) * rows.lh_count + j]);
+  out[seq] = (most + rows.block_size - 1) / rows.block_size;
+}
+
 }  // namespace
+
+cudaError_t launch_blocks_used(const RowMap& rows, const int32_t* n_valid, int32_t* blocks_used, int n_seq,
+                               cudaStream_t st) {
+  blocks_used_kernel<<<static_cast<unsigned>((n_seq + 127) / 128), 128, 0, st>>>(rows, n_valid, blocks_used, n_seq);
+  note_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st) {
   if (p.row_bytes % 16 != 0 || p.row_bytes < 128 || p.row_bytes > CTILE) return cudaErrorInvalidValue;

@@ -86,15 +86,29 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   const int c1 = min((ct + 1) * p.rows_per_cta, n - p.n_recent);
   if (c0 >= c1) return;  // uniform over the CTA
   const int ntiles = (c1 - c0 + TILE_ROWS - 1) / TILE_ROWS;
-  const unsigned char* src =
-      static_cast<const unsigned char*>(p.k) + (s * p.slice_stride + static_cast<int64_t>(c0) * D) * sizeof(T);
+  const unsigned char* kbase = static_cast<const unsigned char*>(p.k);
+  const int64_t sbase = p.rows.slice_base(s);
+  const int32_t* trow = p.rows.seq_table(s);
+  __shared__ int bad_block;
+  if (!p.rows.blocks_ok(trow, c0, c1, &bad_block)) {  // uniform over the CTA
+    if (threadIdx.x == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
+    return;
+  }
 
+  // tile u = rows [c0 + u TILE_ROWS, ...): one bulk copy per run of rows that
+  // are contiguous in memory (the whole tile, or a paged cache's block pieces)
   auto issue = [&](int u) {
-    const int rows = min(TILE_ROWS, c1 - c0 - u * TILE_ROWS);
-    const uint32_t bytes = static_cast<uint32_t>(rows * ROW_BYTES);
+    const int r0 = c0 + u * TILE_ROWS;
+    const int rows = min(TILE_ROWS, c1 - r0);
     uint64_t* bar = &rc.full[u % STAGES];
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(ring + (u % STAGES) * TILE_BYTES, src + static_cast<int64_t>(u) * TILE_BYTES, bytes, bar);
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows * ROW_BYTES));
+    unsigned char* dst = ring + (u % STAGES) * TILE_BYTES;
+    for (int done = 0; done < rows;) {
+      const int run = p.rows.run(r0 + done, rows - done);
+      bulk_g2s(dst + done * ROW_BYTES, kbase + p.rows.row(sbase, trow, r0 + done), static_cast<uint32_t>(run * ROW_BYTES),
+               bar);
+      done += run;
+    }
   };
   if (threadIdx.x == 0) ring_init(rc, ntiles);
   __syncthreads();

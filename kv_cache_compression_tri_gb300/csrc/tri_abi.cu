@@ -37,13 +37,45 @@ tri_status check_kv(const tri_kv* kv, bool need_v) {
   if (!kv->n_valid || !aligned(kv->n_valid, 4)) return TRI_ERR_INVALID_ARG;
   if (!kv->k || !aligned(kv->k, 16)) return TRI_ERR_INVALID_ARG;
   if (need_v && (!kv->v || !aligned(kv->v, 16))) return TRI_ERR_INVALID_ARG;
-  if (kv->slice_stride < static_cast<int64_t>(kv->n_cap) * kv->head_dim) return TRI_ERR_INVALID_ARG;
-  if ((kv->slice_stride * elem_bytes(kv->dtype)) % 16 != 0) return TRI_ERR_INVALID_ARG;
+  const int e = elem_bytes(kv->dtype);
+  if (kv->block_table) {
+    // paged pools: whole blocks of 16-byte aligned rows
+    if (!aligned(kv->block_table, 4)) return TRI_ERR_INVALID_ARG;
+    if (kv->block_size < 16 || kv->block_size % 16 != 0 || kv->n_cap % kv->block_size != 0) return TRI_ERR_INVALID_ARG;
+    if (kv->num_blocks < 1) return TRI_ERR_INVALID_ARG;
+    for (const int64_t st : {kv->block_stride, kv->layer_stride, kv->head_stride})
+      if (st < 0 || (st * e) % 16 != 0) return TRI_ERR_INVALID_ARG;
+    if (kv->head_stride < static_cast<int64_t>(kv->block_size) * kv->head_dim) return TRI_ERR_INVALID_ARG;
+  } else {
+    if (kv->slice_stride < static_cast<int64_t>(kv->n_cap) * kv->head_dim) return TRI_ERR_INVALID_ARG;
+    if ((kv->slice_stride * e) % 16 != 0) return TRI_ERR_INVALID_ARG;
+  }
   if (kv->pos && !aligned(kv->pos, 4)) return TRI_ERR_INVALID_ARG;
   if (kv->pos_out && !aligned(kv->pos_out, 4)) return TRI_ERR_INVALID_ARG;
   if (kv->dev_status && !aligned(kv->dev_status, 4)) return TRI_ERR_INVALID_ARG;
   if (kv->key_layout != TRI_KEYS_PRE_ROPE && kv->key_layout != TRI_KEYS_POST_ROPE) return TRI_ERR_INVALID_ARG;
   return TRI_OK;
+}
+
+// Row addressing of the cache for the kernels.
+RowMap row_map(const tri_kv* kv) {
+  RowMap m{};
+  const int e = elem_bytes(kv->dtype);
+  m.row_bytes = kv->head_dim * e;
+  m.lh_count = kv->n_layers * kv->n_kv_heads;
+  m.n_kv_heads = kv->n_kv_heads;
+  if (kv->block_table) {
+    m.table = kv->block_table;
+    m.block_size = kv->block_size;
+    m.max_blocks = kv->n_cap / kv->block_size;
+    m.num_blocks = kv->num_blocks;
+    m.block_bytes = kv->block_stride * e;
+    m.layer_bytes = kv->layer_stride * e;
+    m.head_bytes = kv->head_stride * e;
+  } else {
+    m.slice_bytes = kv->slice_stride * e;
+  }
+  return m;
 }
 
 // Where the score kernels take each key's rotation from (see launch_score).
@@ -87,7 +119,7 @@ const char* tri_status_string(tri_status s) {
   return "unknown status";
 }
 
-int32_t tri_abi_version(void) { return 2; }
+int32_t tri_abi_version(void) { return 3; }
 
 uint64_t tri_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -190,7 +222,7 @@ tri_status prepare_score(const tri_kv* kv, const tri_centers* c, double rope_the
   p.mrl = c->mrl;
   p.scores = scores;
   p.dev_status = kv->dev_status;
-  p.slice_stride = kv->slice_stride;
+  p.rows = row_map(kv);
   p.n_cap = kv->n_cap;
   p.lh_count = kv->n_layers * kv->n_kv_heads;
   p.n_prompt = n_prompt;
@@ -210,7 +242,7 @@ CompactParams compact_params(const tri_kv* kv, const int32_t* keep_idx, int32_t 
   p.n_valid = kv->n_valid;
   p.keep = keep_idx;
   p.dev_status = kv->dev_status;
-  p.slice_bytes = kv->slice_stride * elem_bytes(kv->dtype);
+  p.rows = row_map(kv);
   p.n_cap = kv->n_cap;
   p.budget = budget;
   p.row_bytes = kv->head_dim * elem_bytes(kv->dtype);
@@ -479,6 +511,14 @@ tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_pro
   p.ucount = ucount;
   p.member_words = u.words;
   e = launch_select_union(p, n_groups, stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status tri_paged_blocks_used(const tri_kv* kv, int32_t* blocks_used, tri_stream_t stream) {
+  tri_status st = check_kv(kv, false);
+  if (st != TRI_OK) return st;
+  if (!kv->block_table || !blocks_used || !aligned(blocks_used, 4)) return TRI_ERR_INVALID_ARG;
+  const cudaError_t e = launch_blocks_used(row_map(kv), kv->n_valid, blocks_used, kv->n_seq, stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 

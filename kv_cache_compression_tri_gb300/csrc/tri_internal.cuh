@@ -180,6 +180,52 @@ __device__ __forceinline__ uint32_t score_key(float x, bool& nan) {
 __device__ __forceinline__ float head_inv_std(float sd) { return sd > 0.f ? 1.0f / sd : 0.f; }
 __device__ __forceinline__ float head_z(float v, float mu, float inv) { return __fmul_rn(__fsub_rn(v, mu), inv); }
 
+// Where the K (or V) row r of slice s lives: contiguous slices at a uniform
+// stride, or a paged pool addressed through the sequence's block table.
+struct RowMap {
+  int64_t slice_bytes;   // contiguous: bytes between slices
+  const int32_t* table;  // paged: [n_seq][max_blocks]; NULL for contiguous slices
+  int32_t block_size, max_blocks, num_blocks;
+  int64_t block_bytes, layer_bytes, head_bytes;
+  int32_t lh_count, n_kv_heads, row_bytes;
+
+  __device__ __forceinline__ bool paged() const { return table != nullptr; }
+  // byte offset of the slice's row 0 (paged: within block 0 of the pool)
+  __device__ __forceinline__ int64_t slice_base(int64_t s) const {
+    if (!table) return s * slice_bytes;
+    const int64_t lh = s % lh_count;
+    return (lh / n_kv_heads) * layer_bytes + (lh % n_kv_heads) * head_bytes;
+  }
+  __device__ __forceinline__ const int32_t* seq_table(int64_t s) const {
+    return table ? table + (s / lh_count) * static_cast<int64_t>(max_blocks) : nullptr;
+  }
+  // byte offset of row r, given slice_base and seq_table of its slice
+  __device__ __forceinline__ int64_t row(int64_t base, const int32_t* trow, int r) const {
+    if (!table) return base + static_cast<int64_t>(r) * row_bytes;
+    return base + static_cast<int64_t>(__ldg(trow + r / block_size)) * block_bytes +
+           static_cast<int64_t>(r % block_size) * row_bytes;
+  }
+  // rows r, r+1, ... that are contiguous in memory (at most `limit`)
+  __device__ __forceinline__ int run(int r, int limit) const {
+    return table ? min(limit, block_size - r % block_size) : limit;
+  }
+  // every table entry for rows [r0, r1) lies in [0, num_blocks) (by the CTA; uniform result)
+  __device__ __forceinline__ bool blocks_ok(const int32_t* trow, int r0, int r1, int* sflag) const {
+    if (!table || r0 >= r1) return true;
+    if (threadIdx.x == 0) *sflag = 0;
+    __syncthreads();
+    for (int b = r0 / block_size + static_cast<int>(threadIdx.x); b <= (r1 - 1) / block_size;
+         b += static_cast<int>(blockDim.x)) {
+      const int v = __ldg(trow + b);
+      if (v < 0 || v >= num_blocks) *sflag = 1;
+    }
+    __syncthreads();
+    const bool ok = *sflag == 0;
+    __syncthreads();
+    return ok;
+  }
+};
+
 // ---------------------------------------------------------------------------
 // Kernel parameter blocks (passed by value).
 // ---------------------------------------------------------------------------
@@ -193,7 +239,7 @@ struct ScoreParams {
   const float* mrl;
   float* scores;
   int32_t* dev_status;
-  int64_t slice_stride;  // elements
+  RowMap rows;  // where the K rows are
   int32_t n_cap;
   int32_t lh_count;  // n_layers * n_kv_heads
   int32_t n_prompt, n_recent;
@@ -252,7 +298,7 @@ struct CompactParams {
   int32_t* n_valid;
   const int32_t* keep;
   int32_t* dev_status;
-  int64_t slice_bytes;  // bytes between slices
+  RowMap rows;  // where the K and V rows are (same layout for both)
   int32_t n_cap;
   int32_t budget;
   int32_t row_bytes;
@@ -298,6 +344,8 @@ cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slice
 cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid, int nv_stride,
                                float* out, int n_blocks, int n_cap, int group, cudaStream_t st);
 cudaError_t launch_union_prep(const UnionPrepParams& q, int n_groups, cudaStream_t st);
+cudaError_t launch_blocks_used(const RowMap& rows, const int32_t* n_valid, int32_t* blocks_used, int n_seq,
+                               cudaStream_t st);
 cudaError_t launch_select_union(const SelectParams& p, int n_groups, cudaStream_t st);
 cudaError_t launch_select_zmax(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st);

@@ -53,7 +53,7 @@ def test_status_strings_and_version(lib):
     for code in range(5):
         assert lib.tri_status_string(code)
     assert lib.tri_status_string(99) == b"unknown status"
-    assert lib.tri_abi_version() == 2
+    assert lib.tri_abi_version() == 3
     assert lib.tri_launch_count() >= 0
 
 
@@ -61,11 +61,17 @@ def _kv(**over):
     import kv_cache_compression_tri_gb300 as tri
     f = dict(k=0x10000, v=0x20000, pos=None, pos_out=0x30000, n_valid=0x40000, slice_stride=128 * 64,
              n_seq=1, n_layers=1, n_kv_heads=2, n_cap=128, head_dim=64, dtype=1, dev_status=None,
-             key_layout=0)
+             key_layout=0, block_table=None, block_size=0, num_blocks=0, block_stride=0, layer_stride=0,
+             head_stride=0)
     f.update(over)
     return tri._TriKV(f["k"], f["v"], f["pos"], f["pos_out"], f["n_valid"], f["slice_stride"],
                       f["n_seq"], f["n_layers"], f["n_kv_heads"], f["n_cap"], f["head_dim"], f["dtype"],
-                      f["dev_status"], f["key_layout"])
+                      f["dev_status"], f["key_layout"], f["block_table"], f["block_size"], f["num_blocks"],
+                      f["block_stride"], f["layer_stride"], f["head_stride"])
+
+
+PAGED = dict(block_table=0xF0000, block_size=16, num_blocks=64, block_stride=2 * 16 * 64, layer_stride=2 * 16 * 64,
+             head_stride=16 * 64, slice_stride=0)
 
 
 INVALID, UNSUPPORTED = 1, 2
@@ -83,6 +89,12 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(n_seq=0), INVALID),
     (dict(pos_out=None), INVALID),  # compaction needs a position target
     (dict(key_layout=2), INVALID),  # neither pre- nor post-RoPE
+    (dict(PAGED, block_size=24), INVALID),  # not a multiple of 16
+    (dict(PAGED, block_size=48), INVALID),  # n_cap 128 not a whole number of blocks
+    (dict(PAGED, num_blocks=0), INVALID),
+    (dict(PAGED, head_stride=4), INVALID),  # rows of one head overlap the next head's
+    (dict(PAGED, block_stride=2 * 16 * 64 + 2), INVALID),  # blocks not 16-byte aligned
+    (dict(PAGED, block_table=0xF0002), INVALID),
 ])
 def test_compact_rejects_bad_cache(lib, over, code):
     kv = _kv(**over)
@@ -178,3 +190,8 @@ def test_gqa_entry_points_reject_bad_args(lib):
     assert sel(stats=None) == INVALID
     assert sel(budget=129) == INVALID
     assert sel(final=0xE0002) == INVALID  # misaligned output
+
+
+def test_paged_blocks_used_needs_a_paged_cache(lib):
+    assert lib.tri_paged_blocks_used(ctypes.byref(_kv()), 0x50000, None) == INVALID
+    assert lib.tri_paged_blocks_used(ctypes.byref(_kv(**PAGED)), None, None) == INVALID
