@@ -626,6 +626,66 @@ def measure_other(args, tri, synth, dev):
     del inp, kh, vh, kv, keep, scores, uws
     torch.cuda.empty_cache()
 
+    # ---- the stack in a paged pool (16-row blocks, shuffled block tables) ---
+    w = synth.WORKLOADS["qwen3_8b_stack"]
+    S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    L, H, d, bs = w.n_layers, w.n_kv_heads, w.head_dim, 16
+    inp = synth.make_inputs(w, dev)
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    mb = w.n_cap // bs
+    nb = w.n_seq * mb
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(1)).view(w.n_seq, mb)
+    table = perm.to(torch.int32).to(dev)
+    kp = torch.empty(nb, L, H, bs, d, dtype=w.dtype, device=dev)
+    vp = torch.empty_like(kp)
+    for sq in range(w.n_seq):  # move each sequence into its blocks, then drop the contiguous copy
+        idx = perm[sq].to(dev)
+        kp[idx] = inp.k[sq].reshape(L, H, mb, bs, d).permute(2, 0, 1, 3, 4)
+        vp[idx] = inp.v[sq].reshape(L, H, mb, bs, d).permute(2, 0, 1, 3, 4)
+    p_cur = inp.p_cur.clone()
+    del inp
+    torch.cuda.empty_cache()
+    head_blocks = table[:, : (B + bs - 1) // bs].reshape(-1).long()  # the blocks compaction rewrites
+    kh, vh = kp[head_blocks].clone(), vp[head_blocks].clone()
+    nv = torch.full((S,), n, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = tri.PagedKVCache(kp, vp, table, nv, None, torch.empty(S, w.n_cap, dtype=torch.int32, device=dev), st)
+    scores = torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
+    keep = torch.empty(S, B, dtype=torch.int32, device=dev)
+    kms = []
+
+    def paged_event():
+        e = [ev() for _ in range(4)]
+        e[0].record()
+        tri.score(kv, c, w.theta, w.offsets, p_cur, scores, n_prompt=P, n_recent=W)
+        e[1].record()
+        tri.select_topk(scores, kv, P, W, B, keep)
+        e[2].record()
+        tri.compact_kv(kv, keep, B)
+        e[3].record()
+        kms.append(e)
+
+    def restore_b():
+        kp[head_blocks] = kh
+        vp[head_blocks] = vh
+        nv.fill_(n)
+
+    ms = timed(paged_event, restore_b)
+    kt = [[x[0].elapsed_time(x[1]), x[1].elapsed_time(x[2]), x[2].elapsed_time(x[3])] for x in kms[args.warmup:]]
+    k_ms = [sum(x[j] for x in kt) / len(kt) for j in range(3)]
+    moved = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
+    score_by = S * (n - P - W) * d * w.elem_bytes
+    by = score_by + moved * (4 * d * w.elem_bytes + 8)
+    assert int(st.item()) == 0
+    out["qwen3_8b_stack_paged"] = {
+        "value": S * n / (ms / 1e3), "unit": UNIT, "ms_per_event": ms, "gbs": by / ms / 1e6,
+        "hbm_frac_of_8tbs": by / ms / 1e6 / 8000.0, "frac_of_measured_peak": by / ms / 1e6 / peak,
+        "algorithmic_bytes": by, "block_size": bs, "layout": "[blocks][layers][kv heads][16 rows][d], shuffled tables",
+        "kernel_ms": {"score": round(k_ms[0], 4), "select": round(k_ms[1], 4), "compact": round(k_ms[2], 4)}}
+    del kp, vp, kh, vh, kv, keep, scores, table
+    torch.cuda.empty_cache()
+
     # ---- the stack with post-RoPE keys (the engine layout) ------------------
     w = synth.WORKLOADS["qwen3_8b_stack_post_rope"]
     S, n, P, W, B = w.n_slices, w.n_valid, w.n_prompt, w.n_recent, w.budget

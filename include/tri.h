@@ -118,7 +118,7 @@ typedef struct {
    * (table entries per sequence) * block_size; slice_stride is ignored. All
    * fields below are ignored when block_table is NULL. */
   const int32_t* block_table; /* device [n_seq][n_cap / block_size], or NULL    */
-  int32_t block_size;         /* rows per block, a multiple of 16                */
+  int32_t block_size;         /* rows per block: a power of two, at least 16      */
   int32_t num_blocks;         /* blocks per pool; every used entry must be below  */
   int64_t block_stride, layer_stride, head_stride; /* elements; x elem size % 16 == 0 */
 } tri_kv;

@@ -36,14 +36,19 @@ constexpr int CSTAGES = 4;
 constexpr int CTILE = 8192;
 constexpr size_t RING_BYTES = CSTAGES * CTILE;
 constexpr size_t COMPACT_SMEM = 2 * RING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
+constexpr int CTAB = 2048;  // paged: table entries cached in shared memory (more are read from global)
 constexpr int POS_PER_THREAD = 8;
 
 // Rows [first, n_keep) of one tensor of one slice, moved by one warp
 // through a ring of CSTAGES tiles of CTILE bytes (see the file comment).
 // Row r of the slice is at pool + rows.row(sbase, trow, r).
+template <bool PAGED>
 __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_t sbase, const int32_t* trow,
-                                          unsigned char* ring, uint64_t* full, const int32_t* keep, int first,
-                                          int n_keep, int rb, int lane, int32_t* dev_status) {
+                                          const int32_t* ctab, unsigned char* ring, uint64_t* full,
+                                          const int32_t* keep, int first, int n_keep, int rb, int lane,
+                                          int32_t* dev_status) {
+  // paged row offsets: from the table cached in shared memory when it fit
+  auto paged_row = [&](int r) { return ctab ? rows.row_cached(sbase, ctab, 0, r) : rows.row(sbase, trow, r); };
   const int TR = CTILE / rb;  // rows per tile
   const int u_first = first / TR;
   const int ntiles = (n_keep - 1) / TR - u_first + 1;
@@ -70,7 +75,8 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
 #pragma unroll
     for (int r = 0; r < RPL; ++r) {
       const int j = lo_j + lane + 32 * r;
-      kv[r] = (k < ntiles && j < hi_j) ? rows.row(sbase, trow, __ldg(keep + j)) : 0;
+      const int src = (k < ntiles && j < hi_j) ? __ldg(keep + j) : 0;
+      kv[r] = PAGED ? paged_row(src) : sbase + static_cast<int64_t>(src) * rb;
     }
   };
   auto gather = [&](int k, const int64_t (&kv)[RPL]) {
@@ -104,10 +110,15 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
       // them that is contiguous in memory (all of them, or per block)
       int lo_j, hi_j, t0;
       rows_of(k, lo_j, hi_j, t0);
-      for (int j = lo_j; j < hi_j;) {
-        const int run = rows.run(j, hi_j - j);
-        bulk_s2g(pool + rows.row(sbase, trow, j), ring + st * CTILE + (j - t0) * rb, static_cast<uint32_t>(run * rb));
-        j += run;
+      if (!PAGED) {
+        bulk_s2g(pool + sbase + static_cast<int64_t>(lo_j) * rb, ring + st * CTILE + (lo_j - t0) * rb,
+                 static_cast<uint32_t>((hi_j - lo_j) * rb));
+      } else {
+        for (int j = lo_j; j < hi_j;) {
+          const int run = rows.run(j, hi_j - j);
+          bulk_s2g(pool + paged_row(j), ring + st * CTILE + (j - t0) * rb, static_cast<uint32_t>(run * rb));
+          j += run;
+        }
       }
       bulk_commit();
     }
@@ -140,6 +151,7 @@ struct CSmem {
   int bad_block;
 };
 
+template <bool PAGED>
 __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ CompactParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ CSmem sm;
@@ -208,7 +220,10 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   // a paged cache: every block the move reads or writes must be in the pool
   const int64_t sbase = p.rows.slice_base(s);
   const int32_t* trow = p.rows.seq_table(s);
-  if (!p.rows.blocks_ok(trow, 0, max(sm.last_src + 1, n_keep), &sm.bad_block)) {
+  const int r1 = max(sm.last_src + 1, n_keep);
+  int32_t* ctab = (PAGED && r1 > 0 && ((r1 - 1) >> p.rows.block_shift) < CTAB)
+                      ? reinterpret_cast<int32_t*>(smem + COMPACT_SMEM) : nullptr;
+  if (PAGED && !p.rows.blocks_ok(trow, 0, r1, &sm.bad_block, ctab)) {
     if (t == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
     return;
   }
@@ -217,7 +232,7 @@ __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ Com
   if (wid < 2) {
     // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
     if (first < n_keep)
-      move_rows(wid == 0 ? p.k : p.v, p.rows, sbase, trow, smem + wid * RING_BYTES,
+      move_rows<PAGED>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, smem + wid * RING_BYTES,
                 reinterpret_cast<uint64_t*>(smem + 2 * RING_BYTES) + wid * CSTAGES, keep, first, n_keep,
                 p.row_bytes, lane, p.dev_status);
     return;
@@ -272,10 +287,12 @@ cudaError_t launch_blocks_used(const RowMap& rows, const int32_t* n_valid, int32
 
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st) {
   if (p.row_bytes % 16 != 0 || p.row_bytes < 128 || p.row_bytes > CTILE) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(COMPACT_SMEM));
+  const bool paged = p.rows.table != nullptr;
+  auto kern = paged ? compact_kernel<true> : compact_kernel<false>;
+  const size_t smem = COMPACT_SMEM + (paged ? CTAB * sizeof(int32_t) : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  compact_kernel<<<static_cast<unsigned>(n_slices), CT, COMPACT_SMEM, st>>>(p);
+  kern<<<static_cast<unsigned>(n_slices), CT, smem, st>>>(p);
   note_launch();
   return cudaGetLastError();
 }

@@ -62,7 +62,7 @@ __device__ __forceinline__ float reduce_scatter(float (&a)[NU], int lane, int& i
   return r;
 }
 
-template <typename T, int D, int STYLE, int PM>
+template <typename T, int D, int STYLE, int PM, bool PAGED>
 __global__ void __launch_bounds__(SCORE_THREADS, 3)
     score_kernel(const __grid_constant__ ScoreParams p) {
   using G = Geo<T, D>;
@@ -89,24 +89,39 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   const unsigned char* kbase = static_cast<const unsigned char*>(p.k);
   const int64_t sbase = p.rows.slice_base(s);
   const int32_t* trow = p.rows.seq_table(s);
-  __shared__ int bad_block;
-  if (!p.rows.blocks_ok(trow, c0, c1, &bad_block)) {  // uniform over the CTA
-    if (threadIdx.x == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
-    return;
+  // paged: the CTA's table entries, checked and cached in shared memory
+  constexpr int TAB = 32 * 128 / 16 + 2;  // entries for the most rows a CTA takes, 16-row blocks
+  __shared__ int32_t stab[PAGED ? TAB : 1];
+  const int b0 = PAGED ? (c0 >> p.rows.block_shift) : 0;
+  if (PAGED) {
+    __shared__ int bad_block;
+    if (!p.rows.blocks_ok(trow, c0, c1, &bad_block, stab)) {  // uniform over the CTA
+      if (threadIdx.x == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
+      return;
+    }
   }
+  const unsigned char* src = kbase + sbase + static_cast<int64_t>(c0) * ROW_BYTES;  // contiguous slices
 
-  // tile u = rows [c0 + u TILE_ROWS, ...): one bulk copy per run of rows that
-  // are contiguous in memory (the whole tile, or a paged cache's block pieces)
+  // Tile u = rows [c0 + u TILE_ROWS, ...): one bulk copy (contiguous slices),
+  // or one per run of rows inside a block (paged). Thread 0 issues while it
+  // also computes, so the contiguous case stays a single copy.
   auto issue = [&](int u) {
     const int r0 = c0 + u * TILE_ROWS;
     const int rows = min(TILE_ROWS, c1 - r0);
     uint64_t* bar = &rc.full[u % STAGES];
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows * ROW_BYTES));
     unsigned char* dst = ring + (u % STAGES) * TILE_BYTES;
-    for (int done = 0; done < rows;) {
-      const int run = p.rows.run(r0 + done, rows - done);
-      bulk_g2s(dst + done * ROW_BYTES, kbase + p.rows.row(sbase, trow, r0 + done), static_cast<uint32_t>(run * ROW_BYTES),
-               bar);
+    if (!PAGED) {
+      bulk_g2s(dst, src + static_cast<int64_t>(u) * TILE_BYTES, static_cast<uint32_t>(rows * ROW_BYTES), bar);
+      return;
+    }
+    // block by block: the first run starts inside a block, the others at row 0
+    const int bs = p.rows.block_size;
+    int b = (r0 >> p.rows.block_shift) - b0, o = r0 & (bs - 1);
+    for (int done = 0; done < rows; ++b, o = 0) {
+      const int run = min(bs - o, rows - done);
+      bulk_g2s(dst + done * ROW_BYTES, kbase + sbase + static_cast<int64_t>(stab[b]) * p.rows.block_bytes + o * ROW_BYTES,
+               static_cast<uint32_t>(run * ROW_BYTES), bar);
       done += run;
     }
   };
@@ -232,9 +247,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
       const int r = c0 + t * TILE_ROWS + rbase + idx * KPW;
       if ((c % (TPK / STEPS)) == 0 && r < c1) __stcs(out + r, v);
     }
-    // This kernel is near its issue limit and keeps its warps in step: the
-    // whole CTA finishes a stage before thread 0 refills it (measured a
-    // little faster here than the per-warp release the heads kernel uses).
+    // The kernel is near its issue limit and keeps its warps in step: the
+    // whole CTA finishes a stage before thread 0 refills it (measured a little
+    // faster here, contiguous or paged, than the per-warp release the heads
+    // kernel uses).
     __syncthreads();
     if (ring_failed(rc)) break;
     if (threadIdx.x == 0 && t + STAGES < ntiles) {
@@ -249,7 +265,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
 
 template <typename T, int D, int STYLE, int PM>
 cudaError_t launch_one(const ScoreParams& p, int n_slices, cudaStream_t st) {
-  auto kern = score_kernel<T, D, STYLE, PM>;
+  auto kern = p.rows.table ? score_kernel<T, D, STYLE, PM, true> : score_kernel<T, D, STYLE, PM, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SCORE_SMEM));
   if (e != cudaSuccess) return e;

@@ -41,7 +41,8 @@ tri_status check_kv(const tri_kv* kv, bool need_v) {
   if (kv->block_table) {
     // paged pools: whole blocks of 16-byte aligned rows
     if (!aligned(kv->block_table, 4)) return TRI_ERR_INVALID_ARG;
-    if (kv->block_size < 16 || kv->block_size % 16 != 0 || kv->n_cap % kv->block_size != 0) return TRI_ERR_INVALID_ARG;
+    const int bsz = kv->block_size;
+    if (bsz < 16 || (bsz & (bsz - 1)) != 0 || kv->n_cap % bsz != 0) return TRI_ERR_INVALID_ARG;  // a power of two
     if (kv->num_blocks < 1) return TRI_ERR_INVALID_ARG;
     for (const int64_t st : {kv->block_stride, kv->layer_stride, kv->head_stride})
       if (st < 0 || (st * e) % 16 != 0) return TRI_ERR_INVALID_ARG;
@@ -67,6 +68,7 @@ RowMap row_map(const tri_kv* kv) {
   if (kv->block_table) {
     m.table = kv->block_table;
     m.block_size = kv->block_size;
+    m.block_shift = __builtin_ctz(static_cast<unsigned>(kv->block_size));
     m.max_blocks = kv->n_cap / kv->block_size;
     m.num_blocks = kv->num_blocks;
     m.block_bytes = kv->block_stride * e;

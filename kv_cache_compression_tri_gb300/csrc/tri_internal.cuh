@@ -185,7 +185,7 @@ __device__ __forceinline__ float head_z(float v, float mu, float inv) { return _
 struct RowMap {
   int64_t slice_bytes;   // contiguous: bytes between slices
   const int32_t* table;  // paged: [n_seq][max_blocks]; NULL for contiguous slices
-  int32_t block_size, max_blocks, num_blocks;
+  int32_t block_size, block_shift, max_blocks, num_blocks;  // block_size = 1 << block_shift
   int64_t block_bytes, layer_bytes, head_bytes;
   int32_t lh_count, n_kv_heads, row_bytes;
 
@@ -202,27 +202,36 @@ struct RowMap {
   // byte offset of row r, given slice_base and seq_table of its slice
   __device__ __forceinline__ int64_t row(int64_t base, const int32_t* trow, int r) const {
     if (!table) return base + static_cast<int64_t>(r) * row_bytes;
-    return base + static_cast<int64_t>(__ldg(trow + r / block_size)) * block_bytes +
-           static_cast<int64_t>(r % block_size) * row_bytes;
+    return base + static_cast<int64_t>(__ldg(trow + (r >> block_shift))) * block_bytes +
+           static_cast<int64_t>(r & (block_size - 1)) * row_bytes;
   }
   // rows r, r+1, ... that are contiguous in memory (at most `limit`)
   __device__ __forceinline__ int run(int r, int limit) const {
-    return table ? min(limit, block_size - r % block_size) : limit;
+    return table ? min(limit, block_size - (r & (block_size - 1))) : limit;
   }
-  // every table entry for rows [r0, r1) lies in [0, num_blocks) (by the CTA; uniform result)
-  __device__ __forceinline__ bool blocks_ok(const int32_t* trow, int r0, int r1, int* sflag) const {
+  // every table entry for rows [r0, r1) lies in [0, num_blocks) (by the CTA;
+  // uniform result). When `cache` is given (room for the entries of blocks
+  // r0 / block_size .. (r1 - 1) / block_size), the entries are kept there.
+  __device__ __forceinline__ bool blocks_ok(const int32_t* trow, int r0, int r1, int* sflag,
+                                            int32_t* cache = nullptr) const {
     if (!table || r0 >= r1) return true;
     if (threadIdx.x == 0) *sflag = 0;
     __syncthreads();
-    for (int b = r0 / block_size + static_cast<int>(threadIdx.x); b <= (r1 - 1) / block_size;
-         b += static_cast<int>(blockDim.x)) {
+    const int b0 = r0 >> block_shift;
+    for (int b = b0 + static_cast<int>(threadIdx.x); b <= ((r1 - 1) >> block_shift); b += static_cast<int>(blockDim.x)) {
       const int v = __ldg(trow + b);
       if (v < 0 || v >= num_blocks) *sflag = 1;
+      if (cache) cache[b - b0] = v;
     }
     __syncthreads();
     const bool ok = *sflag == 0;
     __syncthreads();
     return ok;
+  }
+  // byte offset of row r from a cached table (entry of block b at cache[b - b0])
+  __device__ __forceinline__ int64_t row_cached(int64_t base, const int32_t* cache, int b0, int r) const {
+    return base + static_cast<int64_t>(cache[(r >> block_shift) - b0]) * block_bytes +
+           static_cast<int64_t>(r & (block_size - 1)) * row_bytes;
   }
 };
 

@@ -89,8 +89,10 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(n_seq=0), INVALID),
     (dict(pos_out=None), INVALID),  # compaction needs a position target
     (dict(key_layout=2), INVALID),  # neither pre- nor post-RoPE
-    (dict(PAGED, block_size=24), INVALID),  # not a multiple of 16
-    (dict(PAGED, block_size=48), INVALID),  # n_cap 128 not a whole number of blocks
+    (dict(PAGED, block_size=24), INVALID),  # not a power of two
+    (dict(PAGED, block_size=48), INVALID),
+    (dict(PAGED, block_size=8), INVALID),  # below 16 rows
+    (dict(PAGED, block_size=256), INVALID),  # n_cap 128 not a whole number of blocks
     (dict(PAGED, num_blocks=0), INVALID),
     (dict(PAGED, head_stride=4), INVALID),  # rows of one head overlap the next head's
     (dict(PAGED, block_stride=2 * 16 * 64 + 2), INVALID),  # blocks not 16-byte aligned
