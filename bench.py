@@ -293,7 +293,10 @@ def workload_config(w, path: str = "separate") -> dict:
         "path": ("rand_evict + tri_compact_kv" if w.random else
                  ("tri_compress (score, select, compact in one call)" if path == "compress" else
                   ("tri_score_heads + tri_select_topk_zmax + tri_compact_kv (GQA z-score + max, group %d)"
-                   % w.group if path == "gqa" else "tri_score + tri_select_topk + tri_compact_kv"))),
+                   % w.group if path == "gqa" else
+                   ("tri_score (every row) + tri_select_union + tri_compact_kv" if path == "union" else
+                    ("tri_score + tri_select_topk + tri_compact_kv on a paged pool (16-row blocks)"
+                     if path == "paged" else "tri_score + tri_select_topk + tri_compact_kv"))))),
         "parallelism": "one cache batch per GPU (weak scaling)",
     }
 
@@ -336,7 +339,31 @@ def run_gpu(args, w):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     n_valid = torch.full((S,), n, dtype=torch.int32, device=dev)
     pos_out = torch.empty(S, w.n_cap, dtype=torch.int32, device=dev)
-    kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status, post_rope=(w.key_layout == "post"))
+    union = args.path == "union" and not w.random
+    paged = args.path == "paged"
+    if paged:
+        # the same rows in a block pool: 16-row blocks, one shuffled table per sequence
+        L_, H_, d_, bs = w.n_layers, w.n_kv_heads, w.head_dim, 16
+        mb = w.n_cap // bs
+        perm = torch.randperm(w.n_seq * mb, generator=torch.Generator().manual_seed(1)).view(w.n_seq, mb)
+        kp = torch.empty(w.n_seq * mb, L_, H_, bs, d_, dtype=w.dtype, device=dev)
+        vp = torch.empty_like(kp)
+        for sq in range(w.n_seq):
+            idx = perm[sq].to(dev)
+            kp[idx] = inp.k[sq].reshape(L_, H_, mb, bs, d_).permute(2, 0, 1, 3, 4)
+            vp[idx] = inp.v[sq].reshape(L_, H_, mb, bs, d_).permute(2, 0, 1, 3, 4)
+        del k_head, v_head
+        inp.k = inp.v = None
+        torch.cuda.empty_cache()
+        table = perm.to(torch.int32).to(dev)
+        head_blocks = table[:, : (B + bs - 1) // bs].reshape(-1).long()
+        k_head, v_head = kp[head_blocks].clone(), vp[head_blocks].clone()
+        kv = tri.PagedKVCache(kp, vp, table, n_valid, None, pos_out, status, post_rope=(w.key_layout == "post"))
+    else:
+        kv = tri.KVCache(inp.k, inp.v, n_valid, None, pos_out, status, post_rope=(w.key_layout == "post"))
+    if union:
+        k_head_pick = B - P - W
+        uws = torch.empty(tri.select_union_workspace_bytes(kv, P, W, k_head_pick), dtype=torch.uint8, device=dev)
     fused = (args.path == "compress") and not w.random
     scores = None if (fused or gqa) else torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
     if gqa:
@@ -349,8 +376,12 @@ def run_gpu(args, w):
     stream = torch.cuda.current_stream()
 
     def restore():
-        inp.k[:, :, :, :B].copy_(k_head)
-        inp.v[:, :, :, :B].copy_(v_head)
+        if paged:
+            kp[head_blocks] = k_head
+            vp[head_blocks] = v_head
+        else:
+            inp.k[:, :, :, :B].copy_(k_head)
+            inp.v[:, :, :, :B].copy_(v_head)
         n_valid.fill_(n)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -374,6 +405,11 @@ def run_gpu(args, w):
             tri.score_heads(kv, centers, G, w.theta, w.offsets, inp.p_cur, scores_g, stats, workspace=hws)
             if rec: rec[1].record(stream)
             tri.select_topk_zmax(scores_g, stats, G, kv, P, W, B, keep)
+        elif union:
+            if rec: rec[0].record(stream)
+            tri.score(kv, centers, w.theta, w.offsets, inp.p_cur, scores)  # statistics need every row
+            if rec: rec[1].record(stream)
+            tri.select_union(scores, kv, P, W, B, k_head_pick, keep, workspace=uws)
         else:
             if rec: rec[0].record(stream)
             tri.score(kv, centers, w.theta, w.offsets, inp.p_cur, scores, n_prompt=P, n_recent=W)
@@ -426,7 +462,7 @@ def run_gpu(args, w):
     agg = aggregate(S * n, ws, max_sec, args.steps)
 
     # algorithmic bytes
-    cand_rows = S * n if gqa else S * (n - P - W)  # GQA statistics cover every cached row
+    cand_rows = S * n if (gqa or union) else S * (n - P - W)  # their statistics cover every cached row
     score_bytes = 0 if w.random else cand_rows * d * e
     compact_bytes = moved * (4 * d * e + 8)
     step_bytes = score_bytes + compact_bytes
@@ -461,11 +497,11 @@ def run_gpu(args, w):
     }
     del scores, cws
     torch.cuda.empty_cache()
-    if not args.no_e2e and not gqa:
+    if not args.no_e2e and not (gqa or union or paged):
         result["e2e"] = run_e2e(args, w, tri, synth, inp, centers, dev, stream)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, w)
-    if ws == 1 and not args.no_extra and w.name == "qwen3_8b_stack":
+    if ws == 1 and not args.no_extra and w.name == "qwen3_8b_stack" and args.path == "separate":
         del inp, centers, k_head, v_head, kv, keep, pos_out
         torch.cuda.empty_cache()
         result["other_workloads"] = measure_other(args, tri, synth, dev)
@@ -924,10 +960,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gpu", "reference", "ours"], default="gpu")
     ap.add_argument("--workload", default="qwen3_8b_stack")
-    ap.add_argument("--path", choices=["separate", "compress", "gqa"], default="separate",
+    ap.add_argument("--path", choices=["separate", "compress", "gqa", "union", "paged"], default="separate",
                     help="separate: tri_score + tri_select_topk + tri_compact_kv (per-kernel events); "
                          "compress: the single tri_compress call; gqa: per-query-head scores, "
-                         "z-score + max selection, compaction")
+                         "z-score + max selection, compaction; union: one keep list per (seq, layer) "
+                         "(tri_select_union); paged: the separate calls on a paged copy of the cache "
+                         "(16-row blocks, shuffled tables)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other 32K-token workloads")
