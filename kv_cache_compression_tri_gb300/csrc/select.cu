@@ -213,23 +213,34 @@ __device__ __forceinline__ void block_minmax(SSmem& sm, uint32_t& kmin, uint32_t
   __syncthreads();  // wmin / wmax may be rewritten by the next call
 }
 
-// Window from a systematic sample of the candidates: candidate P + floor((2j
-// + 1) m / (2 NSAMPLE)) for j < NSAMPLE, whose key key_of(slot) gives. The
-// sample keys of ranks r* -+ SAMPLE_SD sd bound [t_lo, t_hi] (r* = need
-// NSAMPLE / m, sd its binomial standard deviation).
-template <class KeyOf>
+// Window from a systematic sample of NSAMPLE candidates spread evenly over
+// [P, n - W), taken as NSAMPLE / RUN runs of RUN consecutive slots (each run
+// RUN-aligned). Sources that read one score row use RUN = 1; sources that
+// read several rows per slot use RUN = 8, one 32-byte sector per row, so the
+// sample touches an eighth of the sectors (their CTAs' rows do not stay in L2
+// until the pass re-reads them). key_of(slot) gives a slot's key. The sample
+// keys of ranks r* -+ SAMPLE_SD sd bound [t_lo, t_hi] (r* = need NSAMPLE / m,
+// sd its binomial standard deviation). Requires m > LCAP (>= 2 NSAMPLE slots).
+template <int RUN, class KeyOf>
 __device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const KeyOf& key_of, uint32_t& t_lo,
                                uint32_t& t_hi) {
+  static_assert(SPT % RUN == 0, "runs per thread");
+  constexpr int NRUN = NSAMPLE / RUN;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   uint32_t sk[SPT];
   uint32_t kmin = 0xffffffffu, kmax = 0u;
+  const int first = (c.P + RUN - 1) / RUN;  // first RUN-aligned run inside the candidates
+  const int last = (c.end - RUN) / RUN;     // last one
 #pragma unroll
-  for (int r = 0; r < SPT; ++r) {
-    const int j = t + NT * r;
-    const int slot = c.P + static_cast<int>(((2LL * j + 1) * m) / (2LL * NSAMPLE));
-    sk[r] = key_of(slot);
-    kmin = min(kmin, sk[r]);
-    kmax = max(kmax, sk[r]);
+  for (int q = 0; q < SPT / RUN; ++q) {
+    const int j = t + NT * q;  // run index
+    const int run = first + static_cast<int>((static_cast<int64_t>(last - first) * j) / (NRUN - 1));
+#pragma unroll
+    for (int r = 0; r < RUN; ++r) {
+      sk[q * RUN + r] = key_of(run * RUN + r);
+      kmin = min(kmin, sk[q * RUN + r]);
+      kmax = max(kmax, sk[q * RUN + r]);
+    }
   }
   block_minmax(sm, kmin, kmax);
   // sample ranks (1 = largest) that bracket the need-th largest candidate
@@ -308,7 +319,7 @@ struct ScoreKeys {
   }
   __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
     const float* r = row;
-    sampled_window(sm, c, need, m, [r](int slot) {
+    sampled_window<1>(sm, c, need, m, [r](int slot) {
       bool ignored = false;  // NaN is flagged by the full pass
       return score_key(__ldcg(r + slot), ignored);
     }, t_lo, t_hi);
@@ -420,7 +431,7 @@ struct ZMaxKeys {
   }
   __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
     const ZMaxKeys& self = *this;
-    sampled_window(sm, c, need, m, [&self](int slot) {
+    sampled_window<8>(sm, c, need, m, [&self](int slot) {
       bool ignored = false;
       return score_key(self.final_score(slot), ignored);
     }, t_lo, t_hi);
@@ -467,7 +478,7 @@ struct UnionKeys {
   }
   __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
     const UnionKeys& self = *this;
-    sampled_window(sm, c, need, m, [&self](int slot) {
+    sampled_window<8>(sm, c, need, m, [&self](int slot) {
       bool ignored = false;
       const bool in_union = (__ldg(self.member + (slot >> 5)) >> (slot & 31)) & 1u;
       return self.key(in_union, self.z.final_score(slot), ignored);

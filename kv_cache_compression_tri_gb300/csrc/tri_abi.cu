@@ -485,11 +485,12 @@ tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_pro
     e = launch_select(select_params(scores, kv, n_prompt, n_recent, u.bk, keepk), n_slices, stream);
     if (e != cudaSuccess) return TRI_ERR_CUDA;
   }
-  UnionPrepParams q{};  // 2. statistics and the union
+  e = launch_slice_stats(scores, kv->n_valid, stats, n_slices, kv->n_cap, stream);  // 2. statistics
+  if (e != cudaSuccess) return TRI_ERR_CUDA;
+  UnionPrepParams q{};  // 3. the union
   q.scores = scores;
   q.n_valid = kv->n_valid;
   q.keepk = keepk;
-  q.stats = stats;
   q.member = member;
   q.ucount = ucount;
   q.dev_status = kv->dev_status;
@@ -506,7 +507,7 @@ tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_pro
                            kv->n_kv_heads, stream);
     if (e != cudaSuccess) return TRI_ERR_CUDA;
   }
-  SelectParams p = select_params(scores, kv, n_prompt, n_recent, budget, keep_idx);  // 3. one list per group
+  SelectParams p = select_params(scores, kv, n_prompt, n_recent, budget, keep_idx);  // 4. one list per group
   p.stats = stats;
   p.group = kv->n_kv_heads;
   p.member = member;

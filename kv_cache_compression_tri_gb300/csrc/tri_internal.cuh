@@ -292,7 +292,6 @@ struct UnionPrepParams {
   const float* scores;    // [S][n_cap], every valid row scored
   const int32_t* n_valid;
   const int32_t* keepk;   // [S][bk]: each slice's own top picks (or NULL when bk == 0)
-  float* stats;           // [S][2] out: mean, std over rows [0, n_valid)
   uint32_t* member;       // [groups][member_words] out
   int32_t* ucount;        // [groups] out
   int32_t* dev_status;
@@ -353,6 +352,8 @@ cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slice
 cudaError_t launch_zmax_scores(const float* scores_g, const float* stats, const int32_t* n_valid, int nv_stride,
                                float* out, int n_blocks, int n_cap, int group, cudaStream_t st);
 cudaError_t launch_union_prep(const UnionPrepParams& q, int n_groups, cudaStream_t st);
+cudaError_t launch_slice_stats(const float* scores, const int32_t* n_valid, float* stats, int n_slices, int n_cap,
+                               cudaStream_t st);
 cudaError_t launch_blocks_used(const RowMap& rows, const int32_t* n_valid, int32_t* blocks_used, int n_seq,
                                cudaStream_t st);
 cudaError_t launch_select_union(const SelectParams& p, int n_groups, cudaStream_t st);

@@ -6,13 +6,14 @@
 // combined score, and topped up by the combined score when it is smaller
 // than the budget. The picks come from the ordinary per-slice selection
 // (select.cu, budget P + W + k_head); the final ranking is the grouped key
-// source of select.cu. Between them this kernel, one CTA per group:
-//   * the mean and standard deviation of each slice's scores over its valid
-//     rows (two passes over the slice: the mean, then the centred squares),
-//     which turn the scores into the z-scores of the combined score
-//     max_h z_h (TriAttention paper summary, "Handling Grouped-Query
-//     Attention": normalise, then take the maximum);
-//   * the union of the heads' picks as a bitmap over the slots, and its size.
+// source of select.cu. Between them:
+//   * slice_stats_kernel, one CTA per slice: the mean and standard deviation
+//     of the slice's scores over its valid rows (two passes over the slice:
+//     the mean, then the centred squares), which turn the scores into the
+//     z-scores of the combined score max_h z_h (TriAttention paper summary,
+//     "Handling Grouped-Query Attention": normalise, then take the maximum);
+//   * union_prep_kernel, one CTA per group: the union of the heads' picks as
+//     a bitmap over the slots, and its size.
 // The heads of a group must hold the same number of rows (their keep list is
 // shared); a group that does not sets TRI_DEV_GROUP_NVALID and keeps nothing
 // from the union.
@@ -64,33 +65,7 @@ __global__ void __launch_bounds__(UT) union_prep_kernel(const __grid_constant__ 
       q.ucount[g] = 0;
     }
     for (int j = t; j < q.member_words; j += UT) member[j] = 0u;
-    for (int h = t; h < q.group; h += UT) {
-      q.stats[(s0 + h) * 2] = 0.f;
-      q.stats[(s0 + h) * 2 + 1] = 0.f;
-    }
     return;
-  }
-
-  // ---- statistics of every slice of the group ------------------------------
-  for (int h = 0; h < q.group; ++h) {
-    const float* row = q.scores + (s0 + h) * static_cast<int64_t>(q.n_cap);
-    float a = 0.f;
-    for (int i = t; i < n; i += UT) a += __ldcg(row + i);
-    const double mean = (n > 0) ? block_sum(a, sred) / n : 0.0;
-    const float mf = static_cast<float>(mean);
-    float b = 0.f;
-    for (int i = t; i < n; i += UT) {
-      const float d = __ldcg(row + i) - mf;
-      b = fmaf(d, d, b);
-    }
-    // the centred sum uses the fp32 mean; correct it to the fp64 one
-    const double dm = mean - static_cast<double>(mf);
-    const double ss = block_sum(b, sred);
-    const double var = (n > 0) ? fmax(ss / n - dm * dm, 0.0) : 0.0;
-    if (t == 0) {
-      q.stats[(s0 + h) * 2] = mf;
-      q.stats[(s0 + h) * 2 + 1] = static_cast<float>(sqrt(var));
-    }
   }
 
   // ---- the union of the heads' own picks ----------------------------------
@@ -114,7 +89,44 @@ __global__ void __launch_bounds__(UT) union_prep_kernel(const __grid_constant__ 
   if (t == 0) q.ucount[g] = static_cast<int32_t>(tot);
 }
 
+// One CTA per slice: mean and population standard deviation of its scores
+// over rows [0, n_valid) -- two passes (the mean, then the centred squares),
+// fp64 block sums in a fixed order.
+__global__ void __launch_bounds__(UT) slice_stats_kernel(const float* __restrict__ scores,
+                                                         const int32_t* __restrict__ n_valid, float* stats,
+                                                         int n_cap) {
+  __shared__ double sred[UW];
+  const int t = threadIdx.x;
+  const int64_t s = blockIdx.x;
+  const int n = min(max(n_valid[s], 0), n_cap);
+  const float* row = scores + s * static_cast<int64_t>(n_cap);
+  float a = 0.f;
+  for (int i = t; i < n; i += UT) a += __ldcg(row + i);
+  const double mean = (n > 0) ? block_sum(a, sred) / n : 0.0;
+  const float mf = static_cast<float>(mean);
+  float b = 0.f;
+  for (int i = t; i < n; i += UT) {
+    const float d = __ldcg(row + i) - mf;
+    b = fmaf(d, d, b);
+  }
+  // the centred sum uses the fp32 mean; correct it to the fp64 one
+  const double dm = mean - static_cast<double>(mf);
+  const double ss = block_sum(b, sred);
+  const double var = (n > 0) ? fmax(ss / n - dm * dm, 0.0) : 0.0;
+  if (t == 0) {
+    stats[s * 2] = mf;
+    stats[s * 2 + 1] = static_cast<float>(sqrt(var));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_slice_stats(const float* scores, const int32_t* n_valid, float* stats, int n_slices, int n_cap,
+                               cudaStream_t st) {
+  slice_stats_kernel<<<static_cast<unsigned>(n_slices), UT, 0, st>>>(scores, n_valid, stats, n_cap);
+  note_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_union_prep(const UnionPrepParams& q, int n_groups, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(q.member_words) * sizeof(uint32_t);

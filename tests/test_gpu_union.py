@@ -43,7 +43,7 @@ def _union_case(w, P, W, B, k_head, nv=None, seed=0):
     final = torch.full((groups, n_cap), 777.0, device="cuda")
     n0 = tri.launch_count()
     tri.select_union(scores, kv, P, W, B, k_head, keep, final_scores=final)
-    assert tri.launch_count() - n0 == (4 if k_head > 0 else 3)
+    assert tri.launch_count() - n0 == (5 if k_head > 0 else 4)
     torch.cuda.synchronize()
     assert int(kv.dev_status.item()) == 0
     g_sc, g_keep, g_fin = scores.cpu().numpy(), keep.cpu().numpy(), final.cpu().numpy()
