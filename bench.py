@@ -290,7 +290,8 @@ def workload_config(w, path: str = "separate") -> dict:
         "n_prompt": w.n_prompt, "n_recent": w.n_recent, "offsets": len(w.offsets),
         "rope_theta": w.theta, "storage": "bf16" if w.elem_bytes == 2 else "f32",
         "keys": "post-RoPE" if w.key_layout == "post" else "pre-RoPE",
-        "path": ("rand_evict + tri_compact_kv" if w.random else
+        "path": (("rand_evict_compact" if path in ("separate", "paged") else "rand_evict + tri_compact_kv")
+                 if w.random else
                  ("tri_compress (score, select, compact in one call)" if path == "compress" else
                   ("tri_score_heads + tri_select_topk_zmax + tri_compact_kv (GQA z-score + max, group %d)"
                    % w.group if path == "gqa" else
@@ -365,6 +366,9 @@ def run_gpu(args, w):
         k_head_pick = B - P - W
         uws = torch.empty(tri.select_union_workspace_bytes(kv, P, W, k_head_pick), dtype=torch.uint8, device=dev)
     fused = (args.path == "compress") and not w.random
+    # Random Attention: rand_evict_compact (selection and compaction in one kernel,
+    # faster there); scored paths: three kernels (the fused one is not faster for them)
+    fused_sc = w.random and args.path in ("separate", "paged")
     scores = None if (fused or gqa) else torch.empty(S, w.n_cap, dtype=torch.float32, device=dev)
     if gqa:
         G = w.group
@@ -393,6 +397,16 @@ def run_gpu(args, w):
             tri.compress(kv, centers, w.theta, w.offsets, inp.p_cur, P, W, B, keep, workspace=cws)
             if rec:
                 rec[1].record(stream)
+                rec[2].record(stream)
+                rec[3].record(stream)
+            return
+        if fused_sc:
+            # Random Attention: the draw, selection and compaction in one kernel per slice
+            if rec:
+                rec[0].record(stream)
+                rec[1].record(stream)
+            tri.rand_evict_compact(kv, 0, 0, P, W, B, keep)
+            if rec:
                 rec[2].record(stream)
                 rec[3].record(stream)
             return
@@ -468,7 +482,9 @@ def run_gpu(args, w):
     step_bytes = score_bytes + compact_bytes
     mean = lambda xs: sum(xs) / len(xs)
     peak, peak_kind = measured_peak_gbs()
-    if w.random:
+    if w.random and fused_sc:
+        dom_name, dom_ms, dom_bytes = "select_compact_kernel", mean(k2_ms), compact_bytes
+    elif w.random:
         dom_name, dom_ms, dom_bytes = "compact_kernel", mean(k3_ms), compact_bytes
     else:
         dom_name, dom_ms, dom_bytes = ("score_heads_kernel" if gqa else "score_kernel"), mean(k1_ms), score_bytes
@@ -485,8 +501,9 @@ def run_gpu(args, w):
         "hbm_frac_of_8tbs": step_bytes / (dev_sec / args.steps) / 1e9 / 8000.0,
         "algorithmic_bytes_per_step": step_bytes,
         "kernel_ms": ({"compress": round(mean(k1_ms), 4)} if fused else
-                      {("score_heads" if gqa else "score") if not w.random else "rand_select": round(mean(k1_ms), 4),
-                       "select": round(mean(k2_ms), 4), "compact": round(mean(k3_ms), 4)}),
+                      ({"rand_evict_compact": round(mean(k2_ms), 4)} if fused_sc else
+                       {("score_heads" if gqa else "score") if not w.random else "rand_select": round(mean(k1_ms), 4),
+                        "select": round(mean(k2_ms), 4), "compact": round(mean(k3_ms), 4)})),
         "moved_rows_per_step": moved,
         "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
@@ -553,7 +570,7 @@ def measure_other(args, tri, synth, dev):
         inp.v[:, :, :, :B].copy_(vh)
         nv.fill_(n)
 
-    ms = timed(lambda: (tri.rand_evict(kv, 0, 0, P, W, B, keep), tri.compact_kv(kv, keep, B)), restore_r)
+    ms = timed(lambda: tri.rand_evict_compact(kv, 0, 0, P, W, B, keep), restore_r)
     moved = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
     by = moved * (4 * w.head_dim * w.elem_bytes + 8)
     assert int(st.item()) == 0
@@ -847,9 +864,23 @@ def measure_other(args, tri, synth, dev):
     return out
 
 
-KERNEL_SOURCES = {"score_kernel": "score.cu", "select_kernel": "select.cu", "compact_kernel": "compact.cu",
-                  "score_heads_kernel": "score_heads.cu",
-                  "rand_select_kernel": "select.cu"}
+# the files each kernel is built from (its traffic record is tied to their hash)
+KERNEL_SOURCES = {"score_kernel": ["score.cu", "score_common.cuh"],
+                  "select_kernel": ["select_core.cuh"],
+                  "compact_kernel": ["compact_core.cuh"],
+                  "score_heads_kernel": ["score_heads.cu", "score_common.cuh"],
+                  "select_compact_kernel": ["select_compact.cu", "select_core.cuh", "compact_core.cuh"]}
+
+
+def kernel_sources_sha1(kernel: str) -> str:
+    """sha1 of the concatenated source files a kernel is built from."""
+    import hashlib
+
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "kv_cache_compression_tri_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def known_traffic(workload: str, kernel: str):
@@ -861,9 +892,7 @@ def known_traffic(workload: str, kernel: str):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(workload, {}).get(kernel)
-        src = os.path.join(ROOT, "kv_cache_compression_tri_gb300", "csrc", KERNEL_SOURCES[kernel])
-        with open(src, "rb") as f:
-            sha = hashlib.sha1(f.read()).hexdigest()
+        sha = kernel_sources_sha1(kernel)
     except (OSError, ValueError, KeyError):
         return None
     if not rec or not sha.startswith(rec.get("source_sha1_prefix", "-")):
@@ -961,7 +990,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gpu", "reference", "ours"], default="gpu")
     ap.add_argument("--workload", default="qwen3_8b_stack")
     ap.add_argument("--path", choices=["separate", "compress", "gqa", "union", "paged"], default="separate",
-                    help="separate: tri_score + tri_select_topk + tri_compact_kv (per-kernel events); "
+                    help="separate: tri_score + tri_select_topk + tri_compact_kv (an event after each; "
+                         "rand_evict_compact for Random Attention); "
                          "compress: the single tri_compress call; gqa: per-query-head scores, "
                          "z-score + max selection, compaction; union: one keep list per (seq, layer) "
                          "(tri_select_union); paged: the separate calls on a paged copy of the cache "

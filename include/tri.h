@@ -275,6 +275,21 @@ tri_status rand_evict_scoped(const tri_kv* kv, uint64_t seed, uint32_t round, tr
                              tri_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tri_select_compact -- exactly tri_select_topk then tri_compact_kv with the
+ * same arguments, each slice selected and compacted by one CTA in a single
+ * launch (one slice's selection overlaps other slices' row traffic; this
+ * pays when selecting is cheap next to the rows moved, as for the Random
+ * Attention draws).
+ * rand_evict_compact -- likewise rand_evict_scoped then tri_compact_kv.
+ * keep_idx is written as by the selection; kv->pos_out required.
+ * ------------------------------------------------------------------------ */
+tri_status tri_select_compact(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
+                              int32_t budget, int32_t* keep_idx, tri_stream_t stream);
+tri_status rand_evict_compact(const tri_kv* kv, uint64_t seed, uint32_t round, tri_draw_scope scope,
+                              int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                              tri_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * tri_compress -- one compression event: score + select + compact.
  * Exactly tri_score (rows [n_prompt, n_valid - n_recent)), tri_select_topk
  * and tri_compact_kv called in sequence with the same arguments (three

@@ -19,7 +19,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "TriError", "KVCache", "PagedKVCache", "paged_blocks_used", "Centers", "lib_path", "load_library", "calibrate_centers",
+    "TriError", "KVCache", "PagedKVCache", "select_compact", "rand_evict_compact", "paged_blocks_used", "Centers", "lib_path", "load_library", "calibrate_centers",
     "calibrate_workspace_bytes", "score", "select_topk", "compact_kv", "rand_evict",
     "compress", "compress_workspace_bytes", "score_heads", "score_heads_workspace_bytes",
     "select_topk_zmax", "select_union", "select_union_workspace_bytes", "rand_evict_scoped", "DRAW_PER_HEAD", "DRAW_PER_LAYER", "DRAW_PER_SEQUENCE",
@@ -116,6 +116,10 @@ def load_library():
         lib.tri_select_union_workspace_bytes.restype = ctypes.c_size_t
         lib.tri_select_union.argtypes = [vp, kvp, i32, i32, i32, i32, vp, vp, vp, ctypes.c_size_t, vp]
         lib.tri_select_union.restype = ctypes.c_int
+        lib.tri_select_compact.argtypes = [vp, kvp, i32, i32, i32, vp, vp]
+        lib.tri_select_compact.restype = ctypes.c_int
+        lib.rand_evict_compact.argtypes = [kvp, u64, u32, ctypes.c_int, i32, i32, i32, vp, vp]
+        lib.rand_evict_compact.restype = ctypes.c_int
         lib.tri_paged_blocks_used.argtypes = [kvp, vp, vp]
         lib.tri_paged_blocks_used.restype = ctypes.c_int
         _lib = lib
@@ -357,6 +361,28 @@ def compact_kv(kv: KVCache, keep: torch.Tensor, budget: int, stream=None) -> Non
     kvs = kv._abi()
     _check("tri_compact_kv", lib.tri_compact_kv(ctypes.byref(kvs), keep.data_ptr(), budget,
                                                 _stream(stream)))
+
+
+def select_compact(scores: torch.Tensor, kv, n_prompt: int, n_recent: int, budget: int, keep: torch.Tensor,
+                   stream=None) -> torch.Tensor:
+    """select_topk then compact_kv, one kernel (tri_select_compact)."""
+    lib = load_library()
+    assert keep.dtype == torch.int32 and keep.is_contiguous() and keep.numel() == kv.n_slices * budget
+    kvs = kv._abi()
+    _check("tri_select_compact", lib.tri_select_compact(scores.data_ptr(), ctypes.byref(kvs), n_prompt, n_recent,
+                                                        budget, keep.data_ptr(), _stream(stream)))
+    return keep
+
+
+def rand_evict_compact(kv, seed: int, rnd: int, n_prompt: int, n_recent: int, budget: int, keep: torch.Tensor,
+                       scope: int = 0, stream=None) -> torch.Tensor:
+    """rand_evict_scoped then compact_kv, one kernel (rand_evict_compact)."""
+    lib = load_library()
+    assert keep.dtype == torch.int32 and keep.is_contiguous() and keep.numel() == kv.n_slices * budget
+    kvs = kv._abi()
+    _check("rand_evict_compact", lib.rand_evict_compact(ctypes.byref(kvs), seed, rnd, scope, n_prompt, n_recent,
+                                                        budget, keep.data_ptr(), _stream(stream)))
+    return keep
 
 
 def compress_workspace_bytes(kv: KVCache) -> int:

@@ -1,270 +1,16 @@
-// compact.cu -- in-place, order-preserving K/V compaction.
-//
-// Random Attention, Appendix F: keep-sets are sorted chronologically and the
-// KV tensors are compacted with a gather. Semantics: for j = 0, 1, ...,
-// n_keep-1 in order, row j <- row keep[j]. keep is ascending with
-// keep[j] >= j, so the source of destination j is never a row written by an
-// earlier destination, though it may be a row that a later destination
-// overwrites (keep = {1, 2, ...}).
-//
-// One CTA owns one slice. After validating the keep list, warp 0 moves the K
-// rows and warp 1 the V rows, each through its own 4-stage ring of 8 KB
-// shared-memory tiles, while warps 2-3 move the positions:
-//   * tile u (destination rows [u*TR, (u+1)*TR)) is gathered row by row with
-//     bulk async copies (TMA, non-tensor) completing on the stage's mbarrier;
-//   * once it has landed it is written back with ONE bulk store: past the
-//     identity prefix (keep[j] == j, e.g. the protected prompt, which is
-//     neither read nor written) every destination row moves, so a tile's
-//     destinations are contiguous;
-//   * the store of tile u overlaps the gathers of tiles u+1..u+3. This is
-//     safe: every source of a later tile is >= (u+1)*TR, above every row tile
-//     u writes, and tile u's own sources were read before its store was
-//     issued.
-// A paged cache (block table per sequence) moves the same logical rows; the
-// physical rows come from the table, and a tile's store is split where its
-// destinations cross a block boundary. Waits on gathers are bounded in
-// wall-clock time (TRI_DEV_TIMEOUT).
+// compact.cu -- the compaction kernel on its own (compact_core.cuh) and the
+// count of blocks a paged cache still uses after it.
 #include <cuda_runtime.h>
 
-#include "tri_internal.cuh"
+#include "compact_core.cuh"
 
 namespace tri {
 namespace {
 
-constexpr int CT = 128;  // threads per CTA: warps 0-1 move K/V rows, warps 2-3 positions
-constexpr int CSTAGES = 4;
-constexpr int CTILE = 8192;
-constexpr size_t RING_BYTES = CSTAGES * CTILE;
-constexpr size_t COMPACT_SMEM = 2 * RING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
-constexpr int CTAB = 2048;  // paged: table entries cached in shared memory (more are read from global)
-constexpr int POS_PER_THREAD = 8;
-
-// Rows [first, n_keep) of one tensor of one slice, moved by one warp
-// through a ring of CSTAGES tiles of CTILE bytes (see the file comment).
-// Row r of the slice is at pool + rows.row(sbase, trow, r).
-template <bool PAGED>
-__device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_t sbase, const int32_t* trow,
-                                          const int32_t* ctab, unsigned char* ring, uint64_t* full,
-                                          const int32_t* keep, int first, int n_keep, int rb, int lane,
-                                          int32_t* dev_status) {
-  // paged row offsets: from the table cached in shared memory when it fit
-  auto paged_row = [&](int r) { return ctab ? rows.row_cached(sbase, ctab, 0, r) : rows.row(sbase, trow, r); };
-  const int TR = CTILE / rb;  // rows per tile
-  const int u_first = first / TR;
-  const int ntiles = (n_keep - 1) / TR - u_first + 1;
-  if (lane == 0) {
-#pragma unroll
-    for (int st = 0; st < CSTAGES; ++st) mbar_init(&full[st], 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
-
-  auto rows_of = [&](int k, int& lo_j, int& hi_j, int& t0) {
-    t0 = (u_first + k) * TR;
-    lo_j = max(t0, first);
-    hi_j = min(t0 + TR, n_keep);
-  };
-  // Each lane copies rows lo_j + lane + 32 r of a tile (r < RPL); the byte
-  // offsets of their sources (keep entry, and block for a paged cache) are
-  // resolved one tile ahead so no gather waits on them.
-  constexpr int RPL = CTILE / 128 / 32;  // most rows a lane copies per tile (2)
-  int64_t knext[RPL];
-  auto load_keep = [&](int k, int64_t (&kv)[RPL]) {
-    int lo_j, hi_j, t0;
-    rows_of(k, lo_j, hi_j, t0);
-#pragma unroll
-    for (int r = 0; r < RPL; ++r) {
-      const int j = lo_j + lane + 32 * r;
-      const int src = (k < ntiles && j < hi_j) ? __ldg(keep + j) : 0;
-      kv[r] = PAGED ? paged_row(src) : sbase + static_cast<int64_t>(src) * rb;
-    }
-  };
-  auto gather = [&](int k, const int64_t (&kv)[RPL]) {
-    int lo_j, hi_j, t0;
-    rows_of(k, lo_j, hi_j, t0);
-    const int st = k % CSTAGES;
-    if (lane == 0) mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((hi_j - lo_j) * rb));
-    __syncwarp();
-#pragma unroll
-    for (int r = 0; r < RPL; ++r) {
-      const int j = lo_j + lane + 32 * r;
-      if (j < hi_j) bulk_g2s(ring + st * CTILE + (j - t0) * rb, pool + kv[r], static_cast<uint32_t>(rb), &full[st]);
-    }
-  };
-
-  for (int k = 0; k < min(CSTAGES - 1, ntiles); ++k) {
-    int64_t kv[RPL];
-    load_keep(k, kv);
-    gather(k, kv);
-  }
-  load_keep(CSTAGES - 1, knext);
-  int k = 0;
-  bool ok = true;
-  for (; k < ntiles; ++k) {
-    const int st = k % CSTAGES;
-    ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / CSTAGES) & 1));
-    ok = __all_sync(FULL_MASK, ok);
-    if (!ok) break;
-    if (lane == 0) {
-      // the tile's destinations are consecutive rows: one store per run of
-      // them that is contiguous in memory (all of them, or per block)
-      int lo_j, hi_j, t0;
-      rows_of(k, lo_j, hi_j, t0);
-      if (!PAGED) {
-        bulk_s2g(pool + sbase + static_cast<int64_t>(lo_j) * rb, ring + st * CTILE + (lo_j - t0) * rb,
-                 static_cast<uint32_t>((hi_j - lo_j) * rb));
-      } else {
-        for (int j = lo_j; j < hi_j;) {
-          const int run = rows.run(j, hi_j - j);
-          bulk_s2g(pool + paged_row(j), ring + st * CTILE + (j - t0) * rb, static_cast<uint32_t>(run * rb));
-          j += run;
-        }
-      }
-      bulk_commit();
-    }
-    const int kn = k + CSTAGES - 1;  // refills the stage of tile k - 1
-    if (kn < ntiles) {
-      int64_t kv[RPL];
-#pragma unroll
-      for (int r = 0; r < RPL; ++r) kv[r] = knext[r];
-      load_keep(kn + 1, knext);
-      if (lane == 0) bulk_wait_read<1>();  // tile k-1's store has read its stage
-      __syncwarp();
-      gather(kn, kv);
-    }
-  }
-  if (!ok && lane == 0) {
-    // A gather never landed: report it and let the copies in flight finish
-    // before the CTA's shared memory is released.
-    set_status(dev_status, TRI_DEV_TIMEOUT);
-    for (int u = k; u < min(ntiles, k + CSTAGES - 1); ++u)
-      (void)mbar_wait_bounded(&full[u % CSTAGES], static_cast<uint32_t>((u / CSTAGES) & 1));
-  }
-  if (lane == 0) bulk_wait_all();
-}
-
-struct CSmem {
-  int bad;
-  int n_keep;
-  int first_move;
-  int last_src;
-  int bad_block;
-};
-
 template <bool PAGED>
 __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ CompactParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ CSmem sm;
-  const int t = threadIdx.x, lane = t & 31;
-  const int64_t s = blockIdx.x;
-  const int32_t* keep = p.keep + s * static_cast<int64_t>(p.budget);
-
-  if (t == 0) {
-    sm.bad = 0;
-    sm.n_keep = p.budget;
-    sm.first_move = p.budget;
-    sm.last_src = -1;
-  }
-  __syncthreads();
-  // Validate the keep list before touching anything: ascending, keep[j] >= j,
-  // < n_cap, and -1 only as trailing padding. Each thread checks runs of 4
-  // entries (one 16-byte load when the list is 16-byte aligned).
-  const bool vec = (p.budget % 4 == 0) && ((reinterpret_cast<uintptr_t>(keep) & 15) == 0);
-  int bad = 0, nk = p.budget, fm = p.budget, ls = -1;
-  for (int j0 = 4 * t; j0 < p.budget; j0 += 4 * CT) {
-    int v[4];
-    if (vec) {
-      const int4 q = __ldg(reinterpret_cast<const int4*>(keep + j0));
-      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = (j0 + e < p.budget) ? __ldg(keep + j0 + e) : -1;
-    }
-    int prev = (j0 > 0) ? __ldg(keep + j0 - 1) : -2;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = j0 + e;
-      if (j >= p.budget) break;
-      const int kj = v[e];
-      if (kj < 0) {
-        bad |= (kj != -1);
-        nk = min(nk, j);
-      } else {
-        bad |= (kj < j || kj >= p.n_cap || (j > 0 && (prev < 0 || prev >= kj)));
-        if (kj != j) fm = min(fm, j);
-        ls = max(ls, kj);
-      }
-      prev = kj;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    bad |= __shfl_xor_sync(FULL_MASK, bad, o);
-    nk = min(nk, __shfl_xor_sync(FULL_MASK, nk, o));
-    fm = min(fm, __shfl_xor_sync(FULL_MASK, fm, o));
-    ls = max(ls, __shfl_xor_sync(FULL_MASK, ls, o));
-  }
-  if (lane == 0) {
-    if (bad) atomicOr(&sm.bad, 1);
-    atomicMin(&sm.n_keep, nk);
-    atomicMin(&sm.first_move, fm);
-    atomicMax(&sm.last_src, ls);
-  }
-  __syncthreads();
-  if (sm.bad) {
-    if (t == 0) set_status(p.dev_status, TRI_DEV_BAD_KEEP);
-    return;
-  }
-  const int n_keep = sm.n_keep;
-  const int first = min(sm.first_move, n_keep);
-  // a paged cache: every block the move reads or writes must be in the pool
-  const int64_t sbase = p.rows.slice_base(s);
-  const int32_t* trow = p.rows.seq_table(s);
-  const int r1 = max(sm.last_src + 1, n_keep);
-  int32_t* ctab = (PAGED && r1 > 0 && ((r1 - 1) >> p.rows.block_shift) < CTAB)
-                      ? reinterpret_cast<int32_t*>(smem + COMPACT_SMEM) : nullptr;
-  if (PAGED && !p.rows.blocks_ok(trow, 0, r1, &sm.bad_block, ctab)) {
-    if (t == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
-    return;
-  }
-
-  const int wid = t >> 5;
-  if (wid < 2) {
-    // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
-    if (first < n_keep)
-      move_rows<PAGED>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, smem + wid * RING_BYTES,
-                reinterpret_cast<uint64_t*>(smem + 2 * RING_BYTES) + wid * CSTAGES, keep, first, n_keep,
-                p.row_bytes, lane, p.dev_status);
-    return;
-  }
-  // warps 2-3 move the positions meanwhile
-  const int pt = t - 64;  // 0 .. PT-1
-  constexpr int PT = CT - 64;
-  int32_t* pos_out = p.pos_out + s * static_cast<int64_t>(p.n_cap);
-  const int32_t* pos_in = p.pos ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
-  if (pos_in == nullptr || pos_in != pos_out) {
-    // distinct buffers (or positions implied by the slot): a plain gather
-    for (int j = pt; j < n_keep; j += PT) pos_out[j] = pos_in ? __ldg(pos_in + __ldg(keep + j)) : __ldg(keep + j);
-  } else {
-    // in place: read a chunk's sources, barrier, write it; sources of later
-    // chunks lie above every row written so far
-    for (int c0 = first; c0 < n_keep; c0 += PT * POS_PER_THREAD) {
-      int32_t v[POS_PER_THREAD];
-#pragma unroll
-      for (int e = 0; e < POS_PER_THREAD; ++e) {
-        const int j = c0 + e * PT + pt;
-        v[e] = (j < n_keep) ? pos_in[__ldg(keep + j)] : 0;
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(PT) : "memory");
-#pragma unroll
-      for (int e = 0; e < POS_PER_THREAD; ++e) {
-        const int j = c0 + e * PT + pt;
-        if (j < n_keep) pos_out[j] = v[e];
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(PT) : "memory");
-    }
-  }
-  if (pt == 0) p.n_valid[s] = n_keep;
+  compact_slice<PAGED, CT>(p, smem, blockIdx.x);
 }
 
 // One thread per sequence: blocks still holding live rows after compaction.

@@ -308,9 +308,45 @@ tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_thet
   const int n_slices = static_cast<int>(slices_of(kv));
   cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, pos_mode(kv), n_slices, stream);
   if (e != cudaSuccess) return TRI_ERR_CUDA;
+  // Selection and compaction as separate kernels: measured faster here than
+  // the fused kernel of tri_select_compact, whose CTAs cannot keep the
+  // copy rate while some of them are selecting.
   e = launch_select(select_params(scores, kv, n_prompt, n_recent, budget, keep_idx), n_slices, stream);
   if (e != cudaSuccess) return TRI_ERR_CUDA;
   e = launch_compact(compact_params(kv, keep_idx, budget), n_slices, stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status tri_select_compact(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
+                              int32_t budget, int32_t* keep_idx, tri_stream_t stream) {
+  tri_status st = check_kv(kv, true);
+  if (st != TRI_OK) return st;
+  if (!kv->pos_out || !scores || !aligned(scores, 4) || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
+  st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
+  const cudaError_t e = launch_select_compact(select_params(scores, kv, n_prompt, n_recent, budget, keep_idx),
+                                              compact_params(kv, keep_idx, budget), false,
+                                              static_cast<int>(slices_of(kv)), stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+tri_status rand_evict_compact(const tri_kv* kv, uint64_t seed, uint32_t round, tri_draw_scope scope,
+                              int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
+                              tri_stream_t stream) {
+  tri_status st = check_kv(kv, true);
+  if (st != TRI_OK) return st;
+  if (kv->n_layers > 65535 || kv->n_kv_heads > 65536) return TRI_ERR_INVALID_ARG;
+  if (scope != TRI_DRAW_PER_HEAD && scope != TRI_DRAW_PER_LAYER && scope != TRI_DRAW_PER_SEQUENCE)
+    return TRI_ERR_INVALID_ARG;
+  if (!kv->pos_out || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
+  st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
+  SelectParams p = select_params(nullptr, kv, n_prompt, n_recent, budget, keep_idx);
+  p.seed = seed;
+  p.round = round;
+  p.draw_scope = scope;
+  const cudaError_t e = launch_select_compact(p, compact_params(kv, keep_idx, budget), true,
+                                              static_cast<int>(slices_of(kv)), stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 

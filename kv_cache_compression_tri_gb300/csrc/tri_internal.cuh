@@ -360,6 +360,10 @@ cudaError_t launch_select_union(const SelectParams& p, int n_groups, cudaStream_
 cudaError_t launch_select_zmax(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, int n_slices, cudaStream_t st);
+// Selection (by score, or by Random Attention draw when `random`) then
+// compaction of each slice in one CTA.
+cudaError_t launch_select_compact(const SelectParams& ps, const CompactParams& pc, bool random, int n_slices,
+                                  cudaStream_t st);
 cudaError_t launch_calibrate(const CalibParams& p, tri_dtype dt, int head_dim,
                              tri_rope_style style, int lh_count, cudaStream_t st);
 int calibrate_split_count(int lh_count, int64_t samples_per_lh);

@@ -73,7 +73,7 @@ def test_paged_score_select_compact_match_contiguous(bs, layout):
     nv[1], nv[5] = 2000, 1500
     inp.n_valid = torch.tensor(nv, dtype=torch.int32, device="cuda")
     c = tri.calibrate_centers(inp.q, w.group)
-    kp, vp, table, kp_full, vp_full = _paged_copy(inp, bs, seed=bs)
+    kp, vp, table, kp_full, vp_full = _paged_copy(inp, bs, seed=bs, layout=layout)
     pos = torch.tensor(np.stack([np.sort(np.random.default_rng(s).choice(3 * n_cap, n_cap, replace=False))
                                  for s in range(S)]), dtype=torch.int32, device="cuda")
     inp.p_cur = torch.full((w.n_seq,), 3 * n_cap + 1, dtype=torch.int64, device="cuda")
@@ -97,6 +97,12 @@ def test_paged_score_select_compact_match_contiguous(bs, layout):
                                pos=pos[s, :n].cpu().numpy().astype(np.int64))
         M = orc.score_bound(k, cm[lh])
         assert np.all(np.abs(sc_p[s, P:n - W].cpu().numpy() - ref[P:n - W]) <= SCORE_TOL * M[P:n - W])
+    # the fused selection + compaction on another paged copy must match the two calls below
+    kp2, vp2, table2, _, _ = _paged_copy(inp, bs, seed=bs + 1, layout=layout)
+    kv_f = tri.PagedKVCache(kp2, vp2, table2, inp.n_valid.clone(), pos.clone(), pos.clone(),
+                            torch.zeros(1, dtype=torch.int32, device="cuda"))
+    keep_f = torch.empty(S, B, dtype=torch.int32, device="cuda")
+    tri.select_compact(sc_p, kv_f, P, W, B, keep_f)
     keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
     tri.select_topk(sc_p, kv_p, P, W, B, keep)
     before = {s: _logical(kp, tab, s, int(nv[s]), L, H, bs).cpu() for s in range(S)}
@@ -122,6 +128,12 @@ def test_paged_score_select_compact_match_contiguous(bs, layout):
         rows_v = before_v[s].view(torch.int16).numpy().copy()
         orc.compact(rows_v, g_keep[s])
         assert np.array_equal(rows_v[:n_keep], _logical(vp, tab, s, n_keep, L, H, bs).cpu().view(torch.int16).numpy())
+    assert torch.equal(keep_f, keep) and torch.equal(kv_f.n_valid, kv_p.n_valid)
+    tab2 = table2.cpu().numpy()
+    for s in range(S):
+        n_keep = int(kv_p.n_valid[s])
+        assert torch.equal(_logical(kp2, tab2, s, n_keep, L, H, bs), _logical(kp, tab, s, n_keep, L, H, bs))
+        assert torch.equal(_logical(vp2, tab2, s, n_keep, L, H, bs), _logical(vp, tab, s, n_keep, L, H, bs))
     # blocks past the table's reach were not written; the tail is free
     assert torch.equal(kp_full[kp.shape[0]:], untouched[0]) and torch.equal(vp_full[kp.shape[0]:], untouched[1])
     assert used.cpu().tolist() == [(B + bs - 1) // bs] * w.n_seq

@@ -336,6 +336,33 @@ def test_random_shared_draw(scope):
     assert not np.array_equal(g0[0], g0[1])
 
 
+@pytest.mark.parametrize("scope", [0, 1])
+def test_rand_evict_compact_equals_two_calls(scope):
+    w = synth.scaled(LAYER, n_seq=2, n_layers=2, n_kv_heads=4, n_cap=3000, n_valid=3000)
+    inp = synth.make_inputs(w, "cuda", with_queries=False)
+    S = w.n_slices
+    nv = np.random.default_rng(8).integers(0, 3001, size=S)
+    nv[0] = 3000
+    k0, v0 = inp.k.clone(), inp.v.clone()
+    out = []
+    for fused in (False, True):
+        kv = tri.KVCache(k0.clone(), v0.clone(), torch.tensor(nv, dtype=torch.int32, device="cuda"), None,
+                         torch.zeros(S, 3000, dtype=torch.int32, device="cuda"),
+                         torch.zeros(1, dtype=torch.int32, device="cuda"))
+        keep = torch.full((S, 900), -5, dtype=torch.int32, device="cuda")
+        if fused:
+            tri.rand_evict_compact(kv, 1234, 2, 100, 0, 900, keep, scope=scope)
+        else:
+            tri.rand_evict_scoped(kv, 1234, 2, scope, 100, 0, 900, keep)
+            tri.compact_kv(kv, keep, 900)
+        torch.cuda.synchronize()
+        assert int(kv.dev_status.item()) == 0
+        out.append((keep, kv))
+    (ka, a), (kb, b) = out
+    assert torch.equal(ka, kb) and torch.equal(a.k, b.k) and torch.equal(a.v, b.v)
+    assert torch.equal(a.n_valid, b.n_valid) and torch.equal(a.pos_out, b.pos_out)
+
+
 def test_nvalid_over_capacity_sets_status():
     w = synth.scaled(TINY, n_kv_heads=2, n_cap=256, n_valid=256, dtype=torch.bfloat16)
     inp = synth.make_inputs(w, "cuda")
@@ -456,13 +483,23 @@ def _compress_vs_separate(w, ragged=False, explicit_pos=False, seed=0, style=0):
     tri.compress(kv_b, c, w.theta, w.offsets, inp.p_cur, P, W, B, keep_b, workspace=ws, style=style)
     torch.cuda.synchronize()
     assert tri.launch_count() - n0 == 3  # score, select, compaction
-    assert int(kv_a.dev_status.item()) == 0 and int(kv_b.dev_status.item()) == 0
-    assert torch.equal(keep_a, keep_b)
-    assert torch.equal(kv_a.k, kv_b.k) and torch.equal(kv_a.v, kv_b.v)
-    assert torch.equal(kv_a.n_valid, kv_b.n_valid)
-    nk = kv_a.n_valid.cpu().numpy()
-    for s in range(S):
-        assert torch.equal(kv_a.pos_out[s, :nk[s]], kv_b.pos_out[s, :nk[s]])
+    # tri_select_compact on the separate call's scores: the same again
+    kv_c = tri.KVCache(k0.clone(), v0.clone(), inp.n_valid.clone(), None if pos is None else pos.clone(),
+                       torch.zeros(S, n_cap, dtype=torch.int32, device="cuda"),
+                       torch.zeros(1, dtype=torch.int32, device="cuda"))
+    if pos is not None:
+        kv_c.pos_out = kv_c.pos
+    keep_c = torch.full((S, B), -5, dtype=torch.int32, device="cuda")
+    tri.select_compact(sc, kv_c, P, W, B, keep_c)
+    torch.cuda.synchronize()
+    for kv_x, keep_x in ((kv_b, keep_b), (kv_c, keep_c)):
+        assert int(kv_a.dev_status.item()) == 0 and int(kv_x.dev_status.item()) == 0
+        assert torch.equal(keep_a, keep_x)
+        assert torch.equal(kv_a.k, kv_x.k) and torch.equal(kv_a.v, kv_x.v)
+        assert torch.equal(kv_a.n_valid, kv_x.n_valid)
+        nk = kv_a.n_valid.cpu().numpy()
+        for s in range(S):
+            assert torch.equal(kv_a.pos_out[s, :nk[s]], kv_x.pos_out[s, :nk[s]])
     # the scores left in the workspace are the separate call's scores
     fs = ws[: S * n_cap * 4].view(torch.float32).view(S, n_cap)
     nv_h = inp.n_valid.cpu().numpy()
