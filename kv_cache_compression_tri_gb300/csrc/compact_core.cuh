@@ -46,7 +46,14 @@ constexpr int POS_PER_THREAD = 8;
 // Rows [first, n_keep) of one tensor of one slice, moved by one warp
 // through a ring of CSTAGES tiles of CTILE bytes (see the file comment).
 // Row r of the slice is at pool + rows.row(sbase, trow, r).
-template <bool PAGED>
+// A keep entry: through the read-only cache when the list is read-only for
+// the whole kernel, else an ordinary load (the fused kernel writes it first).
+template <bool RO>
+__device__ __forceinline__ int keep_at(const int32_t* keep, int j) {
+  return RO ? __ldg(keep + j) : keep[j];
+}
+
+template <bool PAGED, bool RO>
 __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_t sbase, const int32_t* trow,
                                           const int32_t* ctab, unsigned char* ring, uint64_t* full,
                                           const int32_t* keep, int first, int n_keep, int rb, int lane,
@@ -79,7 +86,7 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
 #pragma unroll
     for (int r = 0; r < RPL; ++r) {
       const int j = lo_j + lane + 32 * r;
-      const int src = (k < ntiles && j < hi_j) ? keep[j] : 0;
+      const int src = (k < ntiles && j < hi_j) ? keep_at<RO>(keep, j) : 0;
       kv[r] = PAGED ? paged_row(src) : sbase + static_cast<int64_t>(src) * rb;
     }
   };
@@ -157,9 +164,9 @@ struct CSmem {
 
 // Slice s, by a CTA of NTH threads (NTH >= 128): warps 0 and 1 move the K
 // and V rows, the other warps the positions. smem: COMPACT_SMEM bytes (plus
-// CTAB entries for a paged cache). The keep list is read with ordinary loads:
-// it may have been written earlier in the same kernel.
-template <bool PAGED, int NTH>
+// CTAB entries for a paged cache). RO: the keep list is read-only for the
+// whole kernel (else it was written earlier in the same kernel).
+template <bool PAGED, int NTH, bool RO>
 __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned char* smem, int64_t s) {
   static_assert(NTH >= 128 && NTH % 32 == 0, "compaction CTA");
   __shared__ CSmem sm;
@@ -181,13 +188,14 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   for (int j0 = 4 * t; j0 < p.budget; j0 += 4 * NTH) {
     int v[4];
     if (vec) {
-      const int4 q = *reinterpret_cast<const int4*>(keep + j0);
+      const int4* q4 = reinterpret_cast<const int4*>(keep + j0);
+      const int4 q = RO ? __ldg(q4) : *q4;
       v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = (j0 + e < p.budget) ? keep[j0 + e] : -1;
+      for (int e = 0; e < 4; ++e) v[e] = (j0 + e < p.budget) ? keep_at<RO>(keep, j0 + e) : -1;
     }
-    int prev = (j0 > 0) ? keep[j0 - 1] : -2;
+    int prev = (j0 > 0) ? keep_at<RO>(keep, j0 - 1) : -2;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = j0 + e;
@@ -239,7 +247,7 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   if (wid < 2) {
     // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
     if (first < n_keep)
-      move_rows<PAGED>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, smem + wid * RING_BYTES,
+      move_rows<PAGED, RO>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, smem + wid * RING_BYTES,
                 reinterpret_cast<uint64_t*>(smem + 2 * RING_BYTES) + wid * CSTAGES, keep, first, n_keep,
                 p.row_bytes, lane, p.dev_status);
     return;
@@ -251,7 +259,10 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   const int32_t* pos_in = p.pos ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
   if (pos_in == nullptr || pos_in != pos_out) {
     // distinct buffers (or positions implied by the slot): a plain gather
-    for (int j = pt; j < n_keep; j += PT) pos_out[j] = pos_in ? __ldg(pos_in + keep[j]) : keep[j];
+    for (int j = pt; j < n_keep; j += PT) {
+      const int kj = keep_at<RO>(keep, j);
+      pos_out[j] = pos_in ? __ldg(pos_in + kj) : kj;
+    }
   } else {
     // in place: read a chunk's sources, barrier, write it; sources of later
     // chunks lie above every row written so far
@@ -260,7 +271,7 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
 #pragma unroll
       for (int e = 0; e < POS_PER_THREAD; ++e) {
         const int j = c0 + e * PT + pt;
-        v[e] = (j < n_keep) ? pos_in[keep[j]] : 0;
+        v[e] = (j < n_keep) ? pos_in[keep_at<RO>(keep, j)] : 0;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(PT) : "memory");
 #pragma unroll
