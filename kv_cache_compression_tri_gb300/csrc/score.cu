@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
         if (valid) raw = lds_chunk<T, D, STYLE>(tile + rt * ROW_BYTES, c);
         float re[BPT], im[BPT];
         decode_chunk<T, STYLE>(raw, re, im);
-        float2 a2 = f2(0.f, 0.f);
+        float2 a2;  // starts with the first band pair's product (no zeroing)
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
           const float2 RE = f2(re[2 * q], re[2 * q + 1]);
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
             DR[q] = __ffma2_rn(dr, SR[q], __fmul2_rn(di, NSI[q]));
             DI[q] = __ffma2_rn(dr, SI[q], __fmul2_rn(di, SR[q]));
           }
-          a2 = __ffma2_rn(dr, RE, a2);
+          a2 = (q == 0) ? __fmul2_rn(dr, RE) : __ffma2_rn(dr, RE, a2);
           a2 = __ffma2_rn(di, IM, a2);
           const float2 sq = __ffma2_rn(IM, IM, __fmul2_rn(RE, RE));
           a2 = __ffma2_rn(NW[q], f2(sqrt_approx(sq.x), sqrt_approx(sq.y)), a2);

@@ -222,9 +222,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
         if (valid) raw = lds_chunk<T, D, STYLE>(tile + rt * ROW_BYTES, c);
         float re[BPT], im[BPT];
         decode_chunk<T, STYLE>(raw, re, im);
-        float2 a[GH];
-#pragma unroll
-        for (int g = 0; g < GH; ++g) a[g] = f2(0.f, 0.f);
+        float2 a[GH];  // each starts with the first band pair's product (no zeroing)
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
           const float2 RE = f2(re[2 * q], re[2 * q + 1]);
@@ -235,7 +233,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
             // Re(W e^{i w p_cur} conj(k~)) = Re(W') Re k~ + Im(W') Im k~
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
-              a[g] = __ffma2_rn(WR[g][q], RE, a[g]);
+              a[g] = (q == 0) ? __fmul2_rn(WR[g][q], RE) : __ffma2_rn(WR[g][q], RE, a[g]);
               a[g] = __ffma2_rn(WI[g][q], IM, a[g]);
               a[g] = __ffma2_rn(NW[g][q], mag, a[g]);
             }
@@ -258,7 +256,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
           const float2 zn = __ffma2_rn(er, IM, __fmul2_rn(ei, f2(-RE.x, -RE.y)));
 #pragma unroll
           for (int g = 0; g < GH; ++g) {
-            a[g] = __ffma2_rn(WR[g][q], zr, a[g]);
+            a[g] = (q == 0) ? __fmul2_rn(WR[g][q], zr) : __ffma2_rn(WR[g][q], zr, a[g]);
             a[g] = __ffma2_rn(WI[g][q], zn, a[g]);
             a[g] = __ffma2_rn(NW[g][q], mag, a[g]);
           }
