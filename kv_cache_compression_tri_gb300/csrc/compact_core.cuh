@@ -12,8 +12,9 @@
 // One CTA owns one slice. After validating the keep list, warp 0 moves the K
 // rows and warp 1 the V rows, each through its own 4-stage ring of 8 KB
 // shared-memory tiles, while warps 2-3 move the positions:
-//   * tile u (destination rows [u*TR, (u+1)*TR)) is gathered row by row with
-//     bulk async copies (TMA, non-tensor) completing on the stage's mbarrier;
+//   * tile u (destination rows [u*TR, (u+1)*TR)) is gathered with bulk async
+//     copies (TMA, non-tensor) completing on the stage's mbarrier, one per
+//     run of rows whose sources are adjacent in memory;
 //   * once it has landed it is written back with ONE bulk store: past the
 //     identity prefix (keep[j] == j, e.g. the protected prompt, which is
 //     neither read nor written) every destination row moves, so a tile's
@@ -43,9 +44,6 @@ constexpr size_t COMPACT_SMEM = 2 * RING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
 constexpr int CTAB = 2048;  // paged: table entries cached in shared memory (more are read from global)
 constexpr int POS_PER_THREAD = 8;
 
-// Rows [first, n_keep) of one tensor of one slice, moved by one warp
-// through a ring of CSTAGES tiles of CTILE bytes (see the file comment).
-// Row r of the slice is at pool + rows.row(sbase, trow, r).
 // A keep entry: through the read-only cache when the list is read-only for
 // the whole kernel, else an ordinary load (the fused kernel writes it first).
 template <bool RO>
@@ -53,6 +51,9 @@ __device__ __forceinline__ int keep_at(const int32_t* keep, int j) {
   return RO ? __ldg(keep + j) : keep[j];
 }
 
+// Rows [first, n_keep) of one tensor of one slice, moved by one warp
+// through a ring of CSTAGES tiles of CTILE bytes (see the file comment).
+// Row r of the slice is at pool + rows.row(sbase, trow, r).
 template <bool PAGED, bool RO>
 __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_t sbase, const int32_t* trow,
                                           const int32_t* ctab, unsigned char* ring, uint64_t* full,
@@ -96,10 +97,22 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
     const int st = k % CSTAGES;
     if (lane == 0) mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((hi_j - lo_j) * rb));
     __syncwarp();
+    // Rows lo_j + 32 r + (0..31) sit in lanes 0..31. A row whose source
+    // directly follows the previous lane's source in memory continues that
+    // lane's run; each run is one bulk copy (kept rows are often adjacent
+    // when a large share of the candidates survives).
 #pragma unroll
     for (int r = 0; r < RPL; ++r) {
       const int j = lo_j + lane + 32 * r;
-      if (j < hi_j) bulk_g2s(ring + st * CTILE + (j - t0) * rb, pool + kv[r], static_cast<uint32_t>(rb), &full[st]);
+      const bool valid = j < hi_j;
+      const int64_t prev = __shfl_up_sync(FULL_MASK, kv[r], 1);
+      const bool cont = valid && lane > 0 && kv[r] == prev + rb;
+      const unsigned runs = __ballot_sync(FULL_MASK, cont);
+      if (valid && !cont) {
+        const unsigned after = (lane == 31) ? 0u : (runs >> (lane + 1));  // continuations after this lane
+        const int len = 1 + (__ffs(~after) - 1);
+        bulk_g2s(ring + st * CTILE + (j - t0) * rb, pool + kv[r], static_cast<uint32_t>(len * rb), &full[st]);
+      }
     }
   };
 
