@@ -1,0 +1,222 @@
+"""GPU parity at full size for the rows beyond the basic path, each on the
+Qwen3-8B-shaped stack (16 x 36 x 8 slices, 32768 rows, d 128, bf16) in the
+launch configuration bench.py times:
+
+  * GQA: one score per query head (4 per KV head), z-score + max selection;
+  * post-RoPE keys;
+  * union selection across the 8 KV heads of each (seq, layer);
+  * a paged pool (16-row blocks, shuffled tables) against the contiguous run.
+
+Sampled slices are compared with the oracle (the same tolerances as the
+small cases); every slice is checked for the structural invariants.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import kv_cache_compression_tri_gb300 as tri
+from kv_cache_compression_tri_gb300 import synth
+from gpu_helpers import SCORE_TOL, f64, near_tie_violations, pmap, seq_lh, slice_rows
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+STACK = synth.WORKLOADS["qwen3_8b_stack"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    tri.load_library()
+    yield
+    torch.cuda.empty_cache()
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _structural(keep_all, n, P, W, B):
+    assert np.all(np.diff(keep_all, axis=1) > 0)
+    assert np.all(keep_all[:, :P] == np.arange(P)[None, :])
+    if W:
+        assert np.all(keep_all[:, B - W:] == np.arange(n - W, n)[None, :])
+    assert keep_all.min() >= 0 and keep_all.max() < n
+
+
+def test_gqa_stack_full_size():
+    w = STACK
+    S, n_cap, n, P, W, B, G = w.n_slices, w.n_cap, w.n_valid, w.n_prompt, w.n_recent, w.budget, w.group
+    inp = synth.make_inputs(w, "cuda")
+    cq = tri.calibrate_centers(inp.q, 1)
+    inp.q = None
+    torch.cuda.empty_cache()
+    sample = synth.sample_slices(S, 12)
+    pk = {s: slice_rows(inp.k, s).cpu() for s in sample}
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv = tri.KVCache(inp.k, inp.v, inp.n_valid.clone(), None, torch.empty(S, n_cap, dtype=torch.int32,
+                                                                           device="cuda"), st)
+    sg = torch.empty(S, G, n_cap, device="cuda")
+    stats = torch.empty(S, G, 2, device="cuda")
+    tri.score_heads(kv, cq, G, w.theta, w.offsets, inp.p_cur, sg, stats)
+    keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
+    final = torch.empty(S, n_cap, device="cuda")
+    tri.select_topk_zmax(sg, stats, G, kv, P, W, B, keep, final_scores=final)
+    tri.compact_kv(kv, keep, B)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    keep_all = keep.cpu().numpy()
+    _structural(keep_all, n, P, W, B)
+    c, m, R = f64(cq.center), f64(cq.mean_norm), f64(cq.mrl)
+    g_sc = {s: sg[s].cpu().numpy() for s in sample}
+    g_st = {s: stats[s].cpu().numpy() for s in sample}
+    g_fin = {s: final[s].cpu().numpy() for s in sample}
+    p_cur = inp.p_cur.cpu().numpy()
+
+    def check(s):
+        seq, lh = seq_lh(inp, s)
+        rows = slice(lh * G, (lh + 1) * G)
+        k = pk[s].to(torch.float64).numpy()
+        ref = orc.score_heads(k, c[rows], m[rows], R[rows], w.offsets, int(p_cur[seq]), w.theta)
+        Mg = np.stack([orc.score_bound(k, m[lh * G + g]) for g in range(G)])
+        assert np.all(np.abs(g_sc[s] - ref) <= SCORE_TOL * Mg), s
+        mu, sd, fin = orc.zscore_max(ref)
+        tol_st = SCORE_TOL * Mg.max(axis=1) + 1e-6 * (np.abs(mu) + sd)
+        assert np.all(np.abs(g_st[s][:, 0] - mu) <= tol_st) and np.all(np.abs(g_st[s][:, 1] - sd) <= tol_st)
+        z = (ref - mu[:, None]) / sd[:, None]
+        tol_z = (SCORE_TOL * (Mg + 2 * Mg.max(axis=1)[:, None] * (1 + np.abs(z))) / sd[:, None]).max(axis=0)
+        assert np.all(np.abs(g_fin[s] - fin) <= tol_z), s
+        assert np.array_equal(keep_all[s], orc.select(g_fin[s].astype(np.float64), n, P, W, B)), s
+        problems, _ = near_tie_violations(keep_all[s], fin, tol_z, n, P, W, B, tol=1.0)
+        assert not problems, (s, problems)
+        # compaction bytes
+        rows_np = pk[s].view(torch.int16).numpy().copy()
+        orc.compact(rows_np, keep_all[s])
+        assert np.array_equal(rows_np[:B], slice_rows(kv.k, s)[:B].cpu().view(torch.int16).numpy())
+
+    pmap(check, sample)
+
+
+def test_post_rope_stack_full_size():
+    w = synth.WORKLOADS["qwen3_8b_stack_post_rope"]
+    S, n_cap, n, P, W, B = w.n_slices, w.n_cap, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    inp = synth.make_inputs(w, "cuda")
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    torch.cuda.empty_cache()
+    sample = synth.sample_slices(S, 24)
+    pk = {s: slice_rows(inp.k, s).cpu() for s in sample}
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv = tri.KVCache(inp.k, inp.v, inp.n_valid.clone(), None, torch.empty(S, n_cap, dtype=torch.int32,
+                                                                           device="cuda"), st, post_rope=True)
+    scores = torch.empty(S, n_cap, device="cuda")
+    keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
+    tri.score(kv, c, w.theta, w.offsets, inp.p_cur, scores, n_prompt=P, n_recent=W)
+    tri.select_topk(scores, kv, P, W, B, keep)
+    tri.compact_kv(kv, keep, B)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    keep_all = keep.cpu().numpy()
+    _structural(keep_all, n, P, W, B)
+    cc, cm, cR = f64(c.center), f64(c.mean_norm), f64(c.mrl)
+    g = {s: scores[s].cpu().numpy() for s in sample}
+    p_cur = inp.p_cur.cpu().numpy()
+    slots = np.arange(n)
+
+    def check(s):
+        seq, lh = seq_lh(inp, s)
+        k = pk[s].to(torch.float64).numpy()
+        ref = orc.score_post_rope(k, slots, cc[lh], cm[lh], cR[lh], w.offsets, int(p_cur[seq]), w.theta)
+        M = orc.score_bound(k, cm[lh])
+        lo, hi = P, n - W
+        assert np.all(np.abs(g[s][lo:hi] - ref[lo:hi]) <= SCORE_TOL * M[lo:hi]), s
+        assert np.array_equal(keep_all[s], orc.select(g[s].astype(np.float64), n, P, W, B)), s
+        problems, _ = near_tie_violations(keep_all[s], ref, M, n, P, W, B)
+        assert not problems, (s, problems)
+
+    pmap(check, sample)
+
+
+def test_union_stack_full_size():
+    w = STACK
+    S, n_cap, n, P, W, B, H = w.n_slices, w.n_cap, w.n_valid, w.n_prompt, w.n_recent, w.budget, w.n_kv_heads
+    k_head = B - P - W
+    inp = synth.make_inputs(w, "cuda")
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    torch.cuda.empty_cache()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv = tri.KVCache(inp.k, inp.v, inp.n_valid.clone(), None, torch.empty(S, n_cap, dtype=torch.int32,
+                                                                           device="cuda"), st)
+    scores = torch.empty(S, n_cap, device="cuda")
+    tri.score(kv, c, w.theta, w.offsets, inp.p_cur, scores)
+    keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
+    groups = S // H
+    final = torch.empty(groups, n_cap, device="cuda")
+    tri.select_union(scores, kv, P, W, B, k_head, keep, final_scores=final)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    keep_all = keep.cpu().numpy()
+    _structural(keep_all, n, P, W, B)
+    assert np.all(keep_all.reshape(groups, H, B) == keep_all.reshape(groups, H, B)[:, :1, :])
+    for g in synth.sample_slices(groups, 8):
+        s64 = scores[g * H:(g + 1) * H].cpu().numpy().astype(np.float64)
+        fin = final[g].cpu().numpy()
+        _, _, comb = orc.zscore_max(s64)
+        assert np.all(np.abs(fin - comb) <= 1e-5 * (1 + np.abs(comb) + 50)), g
+        member = orc.union_members(s64, P, W, k_head)
+        assert np.array_equal(keep_all[g * H], orc.union_rank(member, fin.astype(np.float64), P, W, B)), g
+
+
+def test_paged_stack_full_size():
+    w = STACK
+    S, n_cap, n, P, W, B = w.n_slices, w.n_cap, w.n_valid, w.n_prompt, w.n_recent, w.budget
+    L, H, d, bs = w.n_layers, w.n_kv_heads, w.head_dim, 16
+    inp = synth.make_inputs(w, "cuda")
+    c = tri.calibrate_centers(inp.q, w.group)
+    inp.q = None
+    mb = n_cap // bs
+    nb = w.n_seq * mb
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(3)).view(w.n_seq, mb)
+    kp = torch.empty(nb, L, H, bs, d, dtype=w.dtype, device="cuda")
+    vp = torch.empty_like(kp)
+    for sq in range(w.n_seq):
+        idx = perm[sq].cuda()
+        kp[idx] = inp.k[sq].reshape(L, H, mb, bs, d).permute(2, 0, 1, 3, 4)
+        vp[idx] = inp.v[sq].reshape(L, H, mb, bs, d).permute(2, 0, 1, 3, 4)
+    table = perm.to(torch.int32).cuda()
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    kv_p = tri.PagedKVCache(kp, vp, table, inp.n_valid.clone(), None,
+                            torch.empty(S, n_cap, dtype=torch.int32, device="cuda"), st[:1])
+    kv_c = tri.KVCache(inp.k, inp.v, inp.n_valid.clone(), None, torch.empty(S, n_cap, dtype=torch.int32,
+                                                                             device="cuda"), st[1:])
+    keeps = []
+    for kv in (kv_p, kv_c):
+        sc = torch.empty(S, n_cap, device="cuda")
+        keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
+        tri.score(kv, c, w.theta, w.offsets, inp.p_cur, sc, n_prompt=P, n_recent=W)
+        tri.select_topk(sc, kv, P, W, B, keep)
+        tri.compact_kv(kv, keep, B)
+        keeps.append((sc, keep))
+    used = torch.empty(w.n_seq, dtype=torch.int32, device="cuda")
+    tri.paged_blocks_used(kv_p, used)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, 0]
+    (sp, kp_keep), (sc_, kc_keep) = keeps
+    sl = torch.cat([torch.arange(P, n - W, device="cuda")])
+    assert torch.equal(sp[:, sl], sc_[:, sl])  # scores of every candidate row, bit for bit
+    assert torch.equal(kp_keep, kc_keep)
+    assert torch.equal(kv_p.n_valid, kv_c.n_valid) and used.cpu().tolist() == [B // bs] * w.n_seq
+    tab = perm.numpy()
+    for s in synth.sample_slices(S, 16):
+        seq, rem = divmod(s, L * H)
+        layer, head = divmod(rem, H)
+        r = np.arange(B)
+        blk = torch.tensor(tab[seq, r // bs], dtype=torch.long, device="cuda")
+        off = torch.tensor(r % bs, dtype=torch.long, device="cuda")
+        assert torch.equal(kp[blk, layer, head, off], slice_rows(kv_c.k, s)[:B]), s
+        assert torch.equal(vp[blk, layer, head, off], slice_rows(kv_c.v, s)[:B]), s
