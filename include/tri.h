@@ -206,7 +206,8 @@ tri_status tri_calibrate_centers_noalloc(const void* q, tri_dtype dtype, int32_t
  * phase carries the distance).
  * offsets: HOST array of n_offsets (1..64) token offsets (D).
  * p_cur: device [n_seq] int64, position of the newest cached token of each
- * sequence (the current query position). scores: device [n_slices][n_cap]
+ * sequence (the current query position). With a position array (kv->pos),
+ * every valid row's age p_cur - pos[i] must lie in [0, 2^32). scores: device [n_slices][n_cap]
  * fp32. Arithmetic: fp32 FMA; phases in 64-bit fixed-point turns.
  * ------------------------------------------------------------------------ */
 tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,

@@ -37,10 +37,13 @@ __device__ __forceinline__ float2 turns_rotation_accurate(int64_t x, uint64_t nu
 }
 
 // Fast variant (hardware sin/cos on an argument already reduced to
-// [-pi, pi)), for per-key rotations.
+// [-pi, pi)), for per-key rotations. x must lie in [0, 2^32) (a key's age):
+// the top 32 bits of the phase x * nu (mod 2^64) are then exactly
+// hi32(x * nu_lo) + x * nu_hi (mod 2^32), two 32-bit multiplies.
 __device__ __forceinline__ float2 turns_rotation_fast(int64_t x, uint64_t nu) {
-  const uint64_t t = static_cast<uint64_t>(x) * nu;
-  const int32_t hi = static_cast<int32_t>(t >> 32);
+  const uint32_t x32 = static_cast<uint32_t>(x);
+  const uint32_t top = __umulhi(x32, static_cast<uint32_t>(nu)) + x32 * static_cast<uint32_t>(nu >> 32);
+  const int32_t hi = static_cast<int32_t>(top);
   const float ang = static_cast<float>(hi) * 1.4629180792671596e-09f;  // 2 pi / 2^32
   float s, c;
   __sincosf(ang, &s, &c);
