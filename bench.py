@@ -865,11 +865,12 @@ def measure_other(args, tri, synth, dev):
 
 
 # the files each kernel is built from (its traffic record is tied to their hash)
-KERNEL_SOURCES = {"score_kernel": ["score.cu", "score_common.cuh"],
-                  "select_kernel": ["select_core.cuh"],
-                  "compact_kernel": ["compact_core.cuh"],
-                  "score_heads_kernel": ["score_heads.cu", "score_common.cuh"],
-                  "select_compact_kernel": ["select_compact.cu", "select_core.cuh", "compact_core.cuh"]}
+KERNEL_SOURCES = {"score_kernel": ["score.cu", "score_common.cuh", "tri_internal.cuh"],
+                  "select_kernel": ["select_core.cuh", "tri_internal.cuh"],
+                  "compact_kernel": ["compact_core.cuh", "tri_internal.cuh"],
+                  "score_heads_kernel": ["score_heads.cu", "score_common.cuh", "tri_internal.cuh"],
+                  "select_compact_kernel": ["select_compact.cu", "select_core.cuh", "compact_core.cuh",
+                                            "tri_internal.cuh"]}
 
 
 def kernel_sources_sha1(kernel: str) -> str:
@@ -887,8 +888,6 @@ def known_traffic(workload: str, kernel: str):
     """DRAM bytes (read + write) per launch from the committed ncu summary
     (profiles/traffic.json), or None when there is none or the kernel's
     source has changed since the counters were taken."""
-    import hashlib
-
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(workload, {}).get(kernel)
