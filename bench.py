@@ -487,7 +487,8 @@ def run_gpu(args, w):
     elif w.random:
         dom_name, dom_ms, dom_bytes = "compact_kernel", mean(k3_ms), compact_bytes
     else:
-        dom_name, dom_ms, dom_bytes = ("score_heads_kernel" if gqa else "score_kernel"), mean(k1_ms), score_bytes
+        heads_kernel = "score_heads_tc_kernel" if w.dtype == torch.bfloat16 else "score_heads_kernel"
+        dom_name, dom_ms, dom_bytes = (heads_kernel if gqa else "score_kernel"), mean(k1_ms), score_bytes
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = known_traffic(w.name, dom_name)
     result = {
@@ -869,6 +870,7 @@ KERNEL_SOURCES = {"score_kernel": ["score.cu", "score_common.cuh", "tri_internal
                   "select_kernel": ["select_core.cuh", "tri_internal.cuh"],
                   "compact_kernel": ["compact_core.cuh", "tri_internal.cuh"],
                   "score_heads_kernel": ["score_heads.cu", "score_common.cuh", "tri_internal.cuh"],
+                  "score_heads_tc_kernel": ["score_heads_tc.cu", "score_common.cuh", "umma.cuh", "tri_internal.cuh"],
                   "select_compact_kernel": ["select_compact.cu", "select_core.cuh", "compact_core.cuh",
                                             "tri_internal.cuh"]}
 

@@ -18,13 +18,16 @@ constexpr int STAGES = 4;
 constexpr int TILE_BYTES = 16384;
 constexpr size_t RING_BYTES = static_cast<size_t>(STAGES) * TILE_BYTES;
 
-// Control block of a CTA's tile ring, placed after the tiles.
-struct RingCtrl {
-  uint64_t full[STAGES];      // the stage's tile has landed (bulk copy completion)
-  unsigned consumed[STAGES];  // warps done with the stage's current tile
-  int failed;                 // a wait timed out
-  int issued;                 // tiles issued so far
+// Control block of a CTA's tile ring of NST stages read by NW warps, placed
+// after the tiles.
+template <int NST, int NW = SCORE_WARPS>
+struct RingCtrlN {
+  uint64_t full[NST];      // the stage's tile has landed (bulk copy completion)
+  unsigned consumed[NST];  // warps done with the stage's current tile
+  int failed;              // a wait timed out
+  int issued;              // tiles issued so far
 };
+using RingCtrl = RingCtrlN<STAGES>;
 constexpr size_t SCORE_SMEM = RING_BYTES + (sizeof(RingCtrl) + 15) / 16 * 16;
 
 // The ring: consecutive TILE_BYTES chunks of the CTA's rows, each filled by
@@ -36,43 +39,46 @@ constexpr size_t SCORE_SMEM = RING_BYTES + (sizeof(RingCtrl) + 15) / 16 * 16;
 // before the refill, which is issued after a generic-to-async proxy fence.
 
 // Thread 0, before the CTA's first barrier.
-__device__ __forceinline__ void ring_init(RingCtrl& rc, int ntiles) {
+template <int NST, int NW>
+__device__ __forceinline__ void ring_init(RingCtrlN<NST, NW>& rc, int ntiles) {
 #pragma unroll
-  for (int st = 0; st < STAGES; ++st) {
+  for (int st = 0; st < NST; ++st) {
     mbar_init(&rc.full[st], 1);
     rc.consumed[st] = 0u;
   }
   rc.failed = 0;
-  rc.issued = min(STAGES, ntiles);
+  rc.issued = min(NST, ntiles);
   mbar_init_fence();
 }
 
-__device__ __forceinline__ bool ring_failed(const RingCtrl& rc) {
+template <int NST, int NW>
+__device__ __forceinline__ bool ring_failed(const RingCtrlN<NST, NW>& rc) {
   return *reinterpret_cast<const volatile int*>(&rc.failed) != 0;
 }
 
 // Wait for tile t (warp-uniform result); a timeout marks the CTA failed.
-__device__ __forceinline__ bool ring_wait(RingCtrl& rc, int t, int lane) {
-  bool ok = mbar_wait_bounded(&rc.full[t % STAGES], static_cast<uint32_t>((t / STAGES) & 1));
+template <int NST, int NW>
+__device__ __forceinline__ bool ring_wait(RingCtrlN<NST, NW>& rc, int t, int lane) {
+  bool ok = mbar_wait_bounded(&rc.full[t % NST], static_cast<uint32_t>((t / NST) & 1));
   ok = __all_sync(FULL_MASK, ok);
   if (!ok && lane == 0) atomicExch(&rc.failed, 1);
   return ok;
 }
 
 // A warp is done with tile t; the CTA's last warp to get there issues tile
-// t + STAGES into the stage (issue(u) starts the copy of tile u).
-template <class Issue>
-__device__ __forceinline__ void ring_release(RingCtrl& rc, int t, int ntiles, int lane, const Issue& issue) {
+// t + NST into the stage (issue(u) starts the copy of tile u).
+template <int NST, int NW, class Issue>
+__device__ __forceinline__ void ring_release(RingCtrlN<NST, NW>& rc, int t, int ntiles, int lane, const Issue& issue) {
   __syncwarp();
   if (lane == 0) {
     __threadfence_block();
-    if (atomicAdd(&rc.consumed[t % STAGES], 1u) == SCORE_WARPS - 1) {
-      atomicExch(&rc.consumed[t % STAGES], 0u);
+    if (atomicAdd(&rc.consumed[t % NST], 1u) == NW - 1) {
+      atomicExch(&rc.consumed[t % NST], 0u);
       __threadfence_block();
-      if (t + STAGES < ntiles) {
+      if (t + NST < ntiles) {
         fence_proxy_async_smem();
-        issue(t + STAGES);
-        atomicMax(&rc.issued, t + STAGES + 1);
+        issue(t + NST);
+        atomicMax(&rc.issued, t + NST + 1);
       }
     }
   }
@@ -81,12 +87,13 @@ __device__ __forceinline__ void ring_release(RingCtrl& rc, int t, int ntiles, in
 // After the CTA's last barrier: on a timeout, record it and let the copies
 // in flight land before the shared memory is released (the last tile issued
 // into each stage is the newest one there).
-__device__ __forceinline__ void ring_drain(RingCtrl& rc, int32_t* dev_status) {
+template <int NST, int NW>
+__device__ __forceinline__ void ring_drain(RingCtrlN<NST, NW>& rc, int32_t* dev_status) {
   if (threadIdx.x == 0 && ring_failed(rc)) {
     set_status(dev_status, TRI_DEV_TIMEOUT);
     const int is = rc.issued;
-    for (int u = max(0, is - STAGES); u < is; ++u)
-      (void)mbar_wait_bounded(&rc.full[u % STAGES], static_cast<uint32_t>((u / STAGES) & 1));
+    for (int u = max(0, is - NST); u < is; ++u)
+      (void)mbar_wait_bounded(&rc.full[u % NST], static_cast<uint32_t>((u / NST) & 1));
   }
 }
 

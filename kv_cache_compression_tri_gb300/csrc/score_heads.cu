@@ -10,8 +10,10 @@
 // deviation over all cached keys, and a key's final score is the maximum over
 // the G heads (select.cu ranks by it; zmax_scores_kernel writes it out).
 //
-// score_heads_kernel reads every valid row of K once per pass and scores up
-// to four heads per pass (the host launches ceil(G/4) passes). Per band it
+// This file serves fp32 keys (bf16 keys take the tensor-core kernel of
+// score_heads_tc.cu). score_heads_kernel reads every valid row of K once per
+// pass and scores up to four heads per pass (the host launches ceil(G/4)
+// passes). Per band it
 // forms z = e^{i w (p_cur - p)} conj(k) and |k| once; a head then costs two
 // paired FMAs for the trigonometric term (Re(W z) = Re W Re z - Im W Im z)
 // and one for the norm term, so the arithmetic per key grows with the heads
@@ -410,10 +412,7 @@ cudaError_t launch_style(const ScoreParams& p, int n_heads, tri_rope_style style
 
 cudaError_t launch_score_heads(const ScoreParams& p, int n_heads, tri_dtype dt, int head_dim,
                                tri_rope_style style, int pos_mode, int n_slices, cudaStream_t st) {
-  if (dt == TRI_BF16) {
-    if (head_dim == 128) return launch_style<uint16_t, 128>(p, n_heads, style, pos_mode, n_slices, st);
-    return launch_style<uint16_t, 64>(p, n_heads, style, pos_mode, n_slices, st);
-  }
+  if (dt != TRI_F32) return cudaErrorInvalidValue;  // bf16 keys: score_heads_tc.cu
   if (head_dim == 128) return launch_style<float, 128>(p, n_heads, style, pos_mode, n_slices, st);
   return launch_style<float, 64>(p, n_heads, style, pos_mode, n_slices, st);
 }

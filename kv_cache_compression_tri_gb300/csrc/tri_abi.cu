@@ -424,11 +424,24 @@ tri_status tri_score_heads(const tri_kv* kv, const tri_centers* centers, int32_t
   p.partials = static_cast<double*>(ws);
   p.group = group;
   const int n_slices = static_cast<int>(slices_of(kv));
-  for (int h0 = 0; h0 < group; h0 += MAX_HEADS_PER_LAUNCH) {
+  const bool tc = kv->dtype == TRI_BF16;
+  if (tc) {
+    // the tensor-core kernel's own blocks (128 rows) and runs per CTA; never
+    // more CTAs per slice than the workspace query counted (its rotation
+    // steps come from the fixed-point phases on the device)
+    int32_t max_rpc;
+    const ScoreGeometry g = tc_heads_geometry(kv->head_dim, max_rpc);
+    const int32_t cap_rows = (kv->n_cap + g.tile_rows - 1) / g.tile_rows * g.tile_rows;
+    p.rows_per_cta = cap_rows < max_rpc ? cap_rows : max_rpc;
+    p.tiles_per_slice = (kv->n_cap + p.rows_per_cta - 1) / p.rows_per_cta;
+  }
+  const int per_launch = tc ? MAX_HEADS_PER_LAUNCH_TC : MAX_HEADS_PER_LAUNCH;
+  for (int h0 = 0; h0 < group; h0 += per_launch) {
     p.head0 = h0;
-    const int nh = group - h0 < MAX_HEADS_PER_LAUNCH ? group - h0 : MAX_HEADS_PER_LAUNCH;
-    const cudaError_t e = launch_score_heads(p, nh, kv->dtype, kv->head_dim, style, pos_mode(kv),
-                                             n_slices, stream);
+    const int nh = group - h0 < per_launch ? group - h0 : per_launch;
+    const cudaError_t e = tc ? launch_score_heads_tc(p, nh, kv->head_dim, style, pos_mode(kv), n_slices, stream)
+                             : launch_score_heads(p, nh, kv->dtype, kv->head_dim, style, pos_mode(kv),
+                                                  n_slices, stream);
     if (e != cudaSuccess) return TRI_ERR_CUDA;
   }
   const cudaError_t e = launch_heads_stats(p.partials, stats, n_slices, p.tiles_per_slice, group, stream);

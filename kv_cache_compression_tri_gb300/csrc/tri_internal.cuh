@@ -347,10 +347,18 @@ cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st);
 // Per-query-head scores and per-CTA statistics partials, heads [head0, head0 +
 // n_heads) of every group; then the per-(slice, head) mean and standard
 // deviation; then (optional) the z-score maximum of every valid row.
+// fp32 keys: CUDA-core kernel, up to four heads per launch; bf16 keys: the
+// heads' contraction on the tensor cores, up to eight heads per launch.
 constexpr int MAX_HEADS_PER_LAUNCH = 4;
+constexpr int MAX_HEADS_PER_LAUNCH_TC = 8;
 constexpr int MAX_GROUP = 8;
 cudaError_t launch_score_heads(const ScoreParams& p, int n_heads, tri_dtype dt, int head_dim,
                                tri_rope_style style, int pos_mode, int n_slices, cudaStream_t st);
+cudaError_t launch_score_heads_tc(const ScoreParams& p, int n_heads, int head_dim, tri_rope_style style,
+                                  int pos_mode, int n_slices, cudaStream_t st);
+// lane geometry (step, jump, rows per tile) of the tensor-core kernel and its
+// largest run of rows per CTA
+ScoreGeometry tc_heads_geometry(int head_dim, int32_t& max_rows_per_cta);
 cudaError_t launch_heads_stats(const double* partials, float* stats, int n_slices, int tiles_per_slice,
                                int group, cudaStream_t st);
 // out[b][i] = max_g z of rows [b*group, b*group+group) for blocks b < n_blocks;

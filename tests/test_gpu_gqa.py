@@ -64,7 +64,8 @@ def _heads_case(w, style=0, norm_mode=0, explicit_pos=False, ragged=False, P=Non
     n0 = tri.launch_count()
     tri.score_heads(kv, cq, G, w.theta, w.offsets, inp.p_cur, scores_g, stats, style=style,
                     norm_mode=norm_mode)
-    assert tri.launch_count() - n0 == (G + 3) // 4 + 1  # score passes + statistics
+    per_pass = 8 if w.dtype == torch.bfloat16 else 4  # tensor-core kernel for bf16 keys
+    assert tri.launch_count() - n0 == (G + per_pass - 1) // per_pass + 1  # score passes + statistics
     keep = torch.full((S, B), -9, dtype=torch.int32, device="cuda")
     final = torch.full((S, n_cap), 777.0, device="cuda")
     tri.select_topk_zmax(scores_g, stats, G, kv, P, W, B, keep, final_scores=final)
@@ -127,7 +128,7 @@ def test_gqa_layer_workload():
 
 @pytest.mark.parametrize("group", [1, 2, 3, 7, 8])
 def test_gqa_group_sizes(group):
-    # 7 and 8 take two passes over K (4 + 3, 4 + 4); 3 pads the reduction
+    # bf16 keys: one pass over K for up to eight heads (tensor cores)
     w = synth.scaled(LAYER, group=group, n_kv_heads=2, n_layers=2, n_cap=1000, n_valid=1000, n_cal=512,
                      n_prompt=40, n_recent=24, budget=300)
     _heads_case(w, seed=group)
@@ -149,3 +150,22 @@ def test_gqa_constant_scores_and_no_eviction():
     w = synth.scaled(LAYER, n_kv_heads=2, n_cap=600, n_valid=600, n_cal=256, n_prompt=8, n_recent=8, budget=100)
     _heads_case(w, zero_slice=1)
     _heads_case(w, B=600)  # n_valid == budget: nothing evicted
+
+
+def test_gqa_bf16_band_beyond_fp16_range_is_reported():
+    # bf16 keys go through fp16 features: a band of magnitude >= 65520 has no
+    # fp16 value, its scores come out non-finite and the selection says so
+    w = synth.scaled(LAYER, n_kv_heads=2, n_cap=600, n_valid=600, n_cal=256, n_prompt=8, n_recent=8, budget=100)
+    inp = synth.make_inputs(w, "cuda")
+    cq = tri.calibrate_centers(inp.q, 1)
+    slice_rows(inp.k, 1)[300, 0:2] = 2.0e5
+    kv = make_cache(inp)
+    S, G = w.n_slices, w.group
+    scores_g = torch.zeros(S, G, w.n_cap, device="cuda")
+    stats = torch.zeros(S, G, 2, device="cuda")
+    tri.score_heads(kv, cq, G, w.theta, w.offsets, inp.p_cur, scores_g, stats)
+    keep = torch.empty(S, w.budget, dtype=torch.int32, device="cuda")
+    tri.select_topk_zmax(scores_g, stats, G, kv, w.n_prompt, w.n_recent, w.budget, keep)
+    torch.cuda.synchronize()
+    assert int(kv.dev_status.item()) == tri.DEV_NAN_SCORE
+    assert torch.isfinite(scores_g[0]).all()  # the other slice is untouched by it
