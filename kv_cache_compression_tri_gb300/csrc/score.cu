@@ -102,32 +102,38 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   }
   const unsigned char* src = kbase + sbase + static_cast<int64_t>(c0) * ROW_BYTES;  // contiguous slices
 
-  // Tile u = rows [c0 + u TILE_ROWS, ...): one bulk copy (contiguous slices),
-  // or one per run of rows inside a block (paged). Thread 0 issues while it
-  // also computes, so the contiguous case stays a single copy.
+  // Tile u = rows [c0 + u TILE_ROWS, ...): one bulk copy by thread 0
+  // (contiguous slices), or one per run of rows inside a block, issued by the
+  // lanes of warp 0 together (paged).
   auto issue = [&](int u) {
     const int r0 = c0 + u * TILE_ROWS;
     const int rows = min(TILE_ROWS, c1 - r0);
     uint64_t* bar = &rc.full[u % STAGES];
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows * ROW_BYTES));
+    if (!PAGED || lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows * ROW_BYTES));
+    if (PAGED) __syncwarp();
     unsigned char* dst = ring + (u % STAGES) * TILE_BYTES;
     if (!PAGED) {
       bulk_g2s(dst, src + static_cast<int64_t>(u) * TILE_BYTES, static_cast<uint32_t>(rows * ROW_BYTES), bar);
       return;
     }
-    // block by block: the first run starts inside a block, the others at row 0
-    const int bs = p.rows.block_size;
-    int b = (r0 >> p.rows.block_shift) - b0, o = r0 & (bs - 1);
-    for (int done = 0; done < rows; ++b, o = 0) {
-      const int run = min(bs - o, rows - done);
-      bulk_g2s(dst + done * ROW_BYTES, kbase + sbase + static_cast<int64_t>(stab[b]) * p.rows.block_bytes + o * ROW_BYTES,
+    // paged: called by all of warp 0; lane i copies the tile's i-th block
+    // piece (the first starts inside a block, the others at row 0), so the
+    // pieces go out together instead of one after another
+    const int bs = p.rows.block_size, sh = p.rows.block_shift;
+    const int o0 = r0 & (bs - 1);
+    const int nruns = (o0 + rows + bs - 1) >> sh;  // at most TILE_ROWS / 16 + 1
+    if (lane < nruns) {
+      const int start = (lane == 0) ? 0 : lane * bs - o0;  // first row of the piece in the tile
+      const int o = (lane == 0) ? o0 : 0;
+      const int run = min(bs - o, rows - start);
+      bulk_g2s(dst + start * ROW_BYTES,
+               kbase + sbase + static_cast<int64_t>(stab[(r0 >> sh) - b0 + lane]) * p.rows.block_bytes + o * ROW_BYTES,
                static_cast<uint32_t>(run * ROW_BYTES), bar);
-      done += run;
     }
   };
   if (threadIdx.x == 0) ring_init(rc, ntiles);
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (PAGED ? warp == 0 : threadIdx.x == 0) {
     for (int u = 0; u < min(STAGES, ntiles); ++u) issue(u);
   }
 
@@ -253,10 +259,10 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
     // kernel uses).
     __syncthreads();
     if (ring_failed(rc)) break;
-    if (threadIdx.x == 0 && t + STAGES < ntiles) {
+    if ((PAGED ? warp == 0 : threadIdx.x == 0) && t + STAGES < ntiles) {
       fence_proxy_async_smem();
       issue(t + STAGES);
-      rc.issued = t + STAGES + 1;
+      if (threadIdx.x == 0) rc.issued = t + STAGES + 1;
     }
   }
   __syncthreads();
