@@ -294,6 +294,7 @@ __device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const K
 struct ScoreKeys {
   static constexpr int U = 4;  // 16-byte loads in flight per thread
   static constexpr bool GROUPED = false;
+  static constexpr bool INTERIOR = true;  // fetch_interior() for groups inside [P, end)
   const float* row;
   bool vec;  // 16-byte loads allowed
 
@@ -302,6 +303,27 @@ struct ScoreKeys {
     k.row = p.scores + c.s * static_cast<int64_t>(p.n_cap);
     k.vec = (reinterpret_cast<uintptr_t>(k.row) & 15) == 0;  // lo is a multiple of 4
     return k;
+  }
+  // Keys of four slots that all lie in [P, end): one 16-byte load (the row
+  // is 16-byte aligned and i0 a multiple of 4 from it) and the key of each
+  // score in integer operations, equal to score_key's (NaN -> 0 and flagged,
+  // -0 -> +0, then the order-preserving flip).
+  __device__ __forceinline__ uint4 fetch_interior(int i0, bool& nan) const {
+    const uint4 w = __ldcg(reinterpret_cast<const uint4*>(row + i0));
+    const uint32_t b[4] = {w.x, w.y, w.z, w.w};
+    uint32_t k[4];
+    bool any_nan = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t mag = b[e] & 0x7fffffffu;
+      const bool isnan = mag > 0x7f800000u;
+      const uint32_t x = mag ? b[e] : 0u;
+      const uint32_t f = x ^ (static_cast<uint32_t>(static_cast<int32_t>(x) >> 31) | 0x80000000u);
+      k[e] = isnan ? 0u : f;
+      any_nan |= isnan;
+    }
+    nan |= any_nan;
+    return make_uint4(k[0], k[1], k[2], k[3]);
   }
   // Keys of slots i0 .. i0+3 (i0 a multiple of 4 from lo, i0 < end).
   __device__ __forceinline__ uint4 fetch(int i0, int P, int end, bool& nan) const {
@@ -334,6 +356,7 @@ struct ScoreKeys {
 struct DrawKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = false;
+  static constexpr bool INTERIOR = false;
   uint4 ctr;  // counter words 1..3 (head + 65536 layer, seq, round)
   uint2 key;
 
@@ -374,6 +397,7 @@ template <int G>
 struct ZMaxKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = false;
+  static constexpr bool INTERIOR = false;
   const float* base;  // row 0 of the G score rows
   int64_t n_cap;
   float mu[G], inv[G];
@@ -454,6 +478,7 @@ template <int H>
 struct UnionKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = true;
+  static constexpr bool INTERIOR = false;
   ZMaxKeys<H> z;
   const uint32_t* member;  // the group's union bitmap, bit i = slot i
   bool many;
@@ -591,12 +616,30 @@ __device__ __forceinline__ void select_slice(const SelectParams& p, SSmem& sm, i
     unsigned hi = 0u;
     const int ng = (c.end - c.lo + 3) >> 2;
     constexpr int U = Src::U;
+    // groups whose four slots all lie in [P, end): the first one from lo is
+    // a partial group when P is not a multiple of 4, the last one when end
+    // is not
+    const int gin0 = (c.P > c.lo) ? 1 : 0, gin1 = ((c.end - c.lo) >> 2) - 1;
     for (int g0 = t; g0 < ng; g0 += NT * U) {
       uint4 r[U];
+      uint32_t vm[U];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
         const int g = g0 + j * NT;
-        if (g < ng) r[j] = src.fetch(c.lo + 4 * g, c.P, c.end, nan);
+        if (g < ng) {
+          const int i0 = c.lo + 4 * g;
+          bool inner = false;
+          if constexpr (Src::INTERIOR) {
+            inner = src.vec && g >= gin0 && g <= gin1;
+            if (inner) r[j] = src.fetch_interior(i0, nan);
+          }
+          if (inner) {
+            vm[j] = 0xfu;
+          } else {
+            r[j] = src.fetch(i0, c.P, c.end, nan);
+            vm[j] = valid_bits(i0, c.P, c.end);
+          }
+        }
       }
 #pragma unroll
       for (int j = 0; j < U; ++j) {
@@ -604,7 +647,7 @@ __device__ __forceinline__ void select_slice(const SelectParams& p, SSmem& sm, i
         if (g >= ng) break;
         const int i0 = c.lo + 4 * g;
         const uint32_t u[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
-        const uint32_t valid = valid_bits(i0, c.P, c.end);
+        const uint32_t valid = vm[j];
         uint32_t nib = 0u, mid = 0u;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
