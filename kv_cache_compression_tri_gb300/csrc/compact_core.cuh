@@ -10,7 +10,7 @@
 // overwrites (keep = {1, 2, ...}).
 //
 // One CTA owns one slice. After validating the keep list, warp 0 moves the K
-// rows and warp 1 the V rows, each through its own 4-stage ring of 8 KB
+// rows and warp 1 the V rows, each through its own 3-stage ring of 8 KB
 // shared-memory tiles, while warps 2-3 move the positions:
 //   * tile u (destination rows [u*TR, (u+1)*TR)) is gathered with bulk async
 //     copies (TMA, non-tensor) completing on the stage's mbarrier, one per
@@ -19,7 +19,7 @@
 //     identity prefix (keep[j] == j, e.g. the protected prompt, which is
 //     neither read nor written) every destination row moves, so a tile's
 //     destinations are contiguous;
-//   * the store of tile u overlaps the gathers of tiles u+1..u+3. This is
+//   * the store of tile u overlaps the gathers of the following tiles. This is
 //     safe: every source of a later tile is >= (u+1)*TR, above every row tile
 //     u writes, and tile u's own sources were read before its store was
 //     issued.
@@ -37,7 +37,7 @@ namespace tri {
 namespace {
 
 constexpr int CT = 128;  // threads per CTA: warps 0-1 move K/V rows, warps 2-3 positions
-constexpr int CSTAGES = 4;
+constexpr int CSTAGES = 3;
 constexpr int CTILE = 8192;
 constexpr size_t RING_BYTES = CSTAGES * CTILE;
 constexpr size_t COMPACT_SMEM = 2 * RING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
