@@ -324,8 +324,14 @@ tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_thet
  * (rows >= n_valid untouched); stats: device [n_slices][group][2] fp32.
  * ws: device scratch of tri_score_heads_workspace_bytes(kv, group) bytes,
  * 16-byte aligned (fp64 per-CTA partial sums; no initial contents needed).
- * One pass over K computes up to four heads; larger groups take ceil(G/4)
- * passes. The statistics are summed in a fixed order (deterministic).
+ * bf16 keys: one pass over K for the whole group, the contraction over the
+ * heads on the tensor cores with fp16 features (Re z_f, -Im z_f, |k_f|) and
+ * each head's coefficients as an fp16 pair (hi + lo): the score's error is
+ * at most ~2^-11 * sqrt(2) * sum_f E|q(g)_f| |k_f| plus fp32 rounding. A key
+ * band with |k_f| >= 65520 does not fit fp16: its scores come out non-finite
+ * and tri_select_topk_zmax reports TRI_DEV_NAN_SCORE. fp32 keys: fp32
+ * arithmetic on the CUDA cores, up to four heads per pass over K (ceil(G/4)
+ * passes). The statistics are summed in a fixed order (deterministic).
  *
  * tri_select_topk_zmax -- tri_select_topk with the score of candidate i
  * replaced by S_final(i) = max_g (scores_g[s][g][i] - mean_g) / std_g (a head
