@@ -397,7 +397,7 @@ template <int G>
 struct ZMaxKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = false;
-  static constexpr bool INTERIOR = false;
+  static constexpr bool INTERIOR = true;
   const float* base;  // row 0 of the G score rows
   int64_t n_cap;
   float mu[G], inv[G];
@@ -448,6 +448,38 @@ struct ZMaxKeys {
         best[e] = (g == 0) ? z : fmaxf(best[e], z);
       }
     }
+  }
+  // Keys of four slots that all lie in [P, end) (see ScoreKeys): the G
+  // 16-byte loads first, then the same z-score maximum as best4 and
+  // score_key's order in integer operations.
+  __device__ __forceinline__ uint4 fetch_interior(int i0, bool& nan) const {
+    float4 f[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) f[g] = __ldcg(reinterpret_cast<const float4*>(base + g * n_cap + i0));
+    float best[4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float x[4] = {f[g].x, f[g].y, f[g].z, f[g].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float z = head_z(x[e], mu[g], inv[g]);
+        best[e] = (g == 0) ? z : fmaxf(best[e], z);
+      }
+    }
+    uint32_t k[4];
+    bool any_nan = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t b = __float_as_uint(best[e]);
+      const uint32_t mag = b & 0x7fffffffu;
+      const bool isnan = mag > 0x7f800000u;
+      const uint32_t x = mag ? b : 0u;
+      const uint32_t o = x ^ (static_cast<uint32_t>(static_cast<int32_t>(x) >> 31) | 0x80000000u);
+      k[e] = isnan ? 0u : o;
+      any_nan |= isnan;
+    }
+    nan |= any_nan;
+    return make_uint4(k[0], k[1], k[2], k[3]);
   }
   __device__ __forceinline__ uint4 fetch(int i0, int P, int end, bool& nan) const {
     float best[4];
