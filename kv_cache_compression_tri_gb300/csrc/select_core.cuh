@@ -452,11 +452,11 @@ struct ZMaxKeys {
   // Keys of four slots that all lie in [P, end) (see ScoreKeys): the G
   // 16-byte loads first, then the same z-score maximum as best4 and
   // score_key's order in integer operations.
-  __device__ __forceinline__ uint4 fetch_interior(int i0, bool& nan) const {
+  // best4 for four slots inside the row (i0 + 3 < n_cap, vec): all G loads first
+  __device__ __forceinline__ void best4_interior(int i0, float (&best)[4]) const {
     float4 f[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) f[g] = __ldcg(reinterpret_cast<const float4*>(base + g * n_cap + i0));
-    float best[4];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float x[4] = {f[g].x, f[g].y, f[g].z, f[g].w};
@@ -466,6 +466,10 @@ struct ZMaxKeys {
         best[e] = (g == 0) ? z : fmaxf(best[e], z);
       }
     }
+  }
+  __device__ __forceinline__ uint4 fetch_interior(int i0, bool& nan) const {
+    float best[4];
+    best4_interior(i0, best);
     uint32_t k[4];
     bool any_nan = false;
 #pragma unroll
@@ -510,10 +514,11 @@ template <int H>
 struct UnionKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = true;
-  static constexpr bool INTERIOR = false;
+  static constexpr bool INTERIOR = true;
   ZMaxKeys<H> z;
   const uint32_t* member;  // the group's union bitmap, bit i = slot i
   bool many;
+  bool vec;  // 16-byte loads allowed (z.vec)
 
   __device__ static UnionKeys make(const SelectParams& p, const Ctx& c, int, int, int) {
     UnionKeys k;
@@ -521,12 +526,21 @@ struct UnionKeys {
     k.z = ZMaxKeys<H>::at(p, group);
     k.member = p.member + group * p.member_words;
     k.many = p.ucount[group] >= c.B - c.P - c.W;
+    k.vec = k.z.vec;
     return k;
   }
   __device__ __forceinline__ uint32_t key(bool in_union, float comb, bool& nan) const {
     const uint32_t k = score_key(comb, nan);
     if (many) return in_union ? max(k, 1u) : 0u;
     return in_union ? 0xffffffffu : k;
+  }
+  // keys of four slots that all lie in [P, end) (no range checks)
+  __device__ __forceinline__ uint4 fetch_interior(int i0, bool& nan) const {
+    float best[4];
+    z.best4_interior(i0, best);
+    const uint32_t word = __ldg(member + (i0 >> 5)) >> (i0 & 31);  // i0 % 4 == 0: one word
+    return make_uint4(key(word & 1u, best[0], nan), key((word >> 1) & 1u, best[1], nan),
+                      key((word >> 2) & 1u, best[2], nan), key((word >> 3) & 1u, best[3], nan));
   }
   __device__ __forceinline__ uint4 fetch(int i0, int P, int end, bool& nan) const {
     float best[4];
