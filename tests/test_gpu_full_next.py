@@ -3,6 +3,7 @@ Qwen3-8B-shaped stack (16 x 36 x 8 slices, 32768 rows, d 128, bf16) in the
 launch configuration bench.py times:
 
   * GQA: one score per query head (4 per KV head), z-score + max selection;
+    and a group of 8 heads with explicit positions and ragged row counts;
   * post-RoPE keys;
   * union selection across the 8 KV heads of each (seq, layer);
   * a paged pool (16-row blocks, shuffled tables) against the contiguous run.
@@ -99,6 +100,59 @@ def test_gqa_stack_full_size():
         assert np.array_equal(rows_np[:B], slice_rows(kv.k, s)[:B].cpu().view(torch.int16).numpy())
 
     pmap(check, sample)
+
+
+def test_gqa_eight_heads_explicit_positions_long_slices():
+    # the tensor-core kernel with a full group of eight heads (one pass, four
+    # heads per read-out warp), explicit positions, ragged row counts and two
+    # CTAs per slice, against the oracle on every slice
+    w = synth.scaled(STACK, n_seq=1, n_layers=2, group=8, n_cal=1024)
+    S, n_cap, P, W, B, G = w.n_slices, w.n_cap, w.n_prompt, w.n_recent, w.budget, w.group
+    inp = synth.make_inputs(w, "cuda")
+    cq = tri.calibrate_centers(inp.q, 1)
+    inp.q = None
+    rng = np.random.default_rng(8)
+    nv = rng.integers(B + 1, n_cap + 1, size=S)
+    nv[0], nv[-1] = n_cap, B + 1
+    n_valid = torch.tensor(nv, dtype=torch.int32, device="cuda")
+    pos_np = np.stack([np.sort(rng.choice(4 * n_cap, size=n_cap, replace=False)) for _ in range(S)]).astype(np.int32)
+    pos = torch.tensor(pos_np, device="cuda")
+    p_cur = torch.full((w.n_seq,), 4 * n_cap + 3, dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv = tri.KVCache(inp.k, inp.v, n_valid, pos, torch.empty(S, n_cap, dtype=torch.int32, device="cuda"), st)
+    sg = torch.full((S, G, n_cap), 12345.0, device="cuda")
+    stats = torch.empty(S, G, 2, device="cuda")
+    tri.score_heads(kv, cq, G, w.theta, w.offsets, p_cur, sg, stats)
+    keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
+    final = torch.empty(S, n_cap, device="cuda")
+    tri.select_topk_zmax(sg, stats, G, kv, P, W, B, keep, final_scores=final)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    c, m, R = f64(cq.center), f64(cq.mean_norm), f64(cq.mrl)
+    g_sc, g_st, g_fin, keep_all = sg.cpu().numpy(), stats.cpu().numpy(), final.cpu().numpy(), keep.cpu().numpy()
+    ks = {s: slice_rows(inp.k, s).cpu().to(torch.float64).numpy() for s in range(S)}
+
+    def check(s):
+        n = int(nv[s])
+        _, lh = seq_lh(inp, s)
+        rows = slice(lh * G, (lh + 1) * G)
+        k = ks[s][:n]
+        ref = orc.score_heads(k, c[rows], m[rows], R[rows], w.offsets, int(p_cur[0]), w.theta,
+                              pos=pos_np[s, :n].astype(np.int64))
+        Mg = np.stack([orc.score_bound(k, m[lh * G + g]) for g in range(G)])
+        assert np.all(np.abs(g_sc[s, :, :n] - ref) <= SCORE_TOL * Mg), s
+        assert np.all(g_sc[s, :, n:] == 12345.0)
+        mu, sd, fin = orc.zscore_max(ref)
+        tol_st = SCORE_TOL * Mg.max(axis=1) + 1e-6 * (np.abs(mu) + sd)
+        assert np.all(np.abs(g_st[s, :, 0] - mu) <= tol_st) and np.all(np.abs(g_st[s, :, 1] - sd) <= tol_st)
+        z = (ref - mu[:, None]) / sd[:, None]
+        tol_z = (SCORE_TOL * (Mg + 2 * Mg.max(axis=1)[:, None] * (1 + np.abs(z))) / sd[:, None]).max(axis=0)
+        assert np.all(np.abs(g_fin[s, :n] - fin) <= tol_z), s
+        assert np.array_equal(keep_all[s], orc.select(g_fin[s, :n].astype(np.float64), n, P, W, B)), s
+        problems, _ = near_tie_violations(keep_all[s], fin, tol_z, n, P, W, B, tol=1.0)
+        assert not problems, (s, problems)
+
+    pmap(check, list(range(S)))
 
 
 def test_post_rope_stack_full_size():
