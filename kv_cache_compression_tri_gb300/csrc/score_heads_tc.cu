@@ -27,22 +27,34 @@
 //
 // CTA: one per SM, a run of up to 16384 rows of one slice, with two groups
 // of eight feature warps, an MMA warp and a copy warp. The copy warp streams
-// key tiles of 128 rows into a ring (bulk async copies completing on "full"
-// mbarriers; a stage is refilled once its "empty" mbarrier says the tile was
-// used). Each tile is one MMA block, and the two groups take alternate
-// tiles, each with its own feature buffer and accumulator: while one group
-// waits for its block's MMAs the other forms features, so the waits of one
-// overlap the arithmetic of the other. A group forms the features of its
-// block t in the operands' 128-byte-swizzled K-major layout and arrives on
-// "A full"; the MMA warp issues the block's MMAs into the group's
-// accumulator and commits them to "MMA done"; before forming block t + 2 in
-// the same buffer the group reads block t's accumulator -- each warp 32 keys
-// (its quarter of the tensor-memory lanes) and half of the heads -- stores
-// the scores, adds them to the heads' statistics (sum and sum of squares
-// shifted by the thread's first value, folded in fp64 in a fixed order into
-// one partial per CTA and head, as score_heads.cu does) and arrives on
-// "D free", which the MMA warp waits for before it overwrites that
-// accumulator. No CTA barrier in the loop; every wait is bounded.
+// key tiles of 128 rows into a 64 KB ring (bulk async copies completing on
+// "full" mbarriers; a stage is refilled once its "empty" mbarrier says the
+// tile was taken). Each tile is one MMA block; the two groups take
+// alternate tiles. A group first loads its lanes' chunks of the tile into
+// registers and hands the stage back, so the ring's bytes stay in flight
+// rather than waiting for arithmetic. Blocks rotate through three operand
+// buffers and three accumulators (block t uses buffer t % 3): the group
+// forms the features of block t in the operands' 128-byte-swizzled K-major
+// layout once block t - 3 (the other group's) is done with that buffer, and
+// arrives on "A full"; the MMA warp issues the block's MMAs into accumulator
+// t % 3 and commits them to "MMA done"; the group then reads out its
+// previous block t - 2, whose MMAs ran while it formed block t -- each warp
+// 32 keys (its quarter of the tensor-memory lanes) and half of the heads --
+// stores the scores, adds them to the heads' statistics (sum and sum of
+// squares shifted by the thread's first value, folded in fp64 in a fixed
+// order into one partial per CTA and head, as score_heads.cu does) and
+// arrives on "D free", which the MMA warp waits for before block t + 1
+// overwrites that accumulator. No group waits for its own block's MMAs, no
+// CTA barrier in the loop; every wait is bounded.
+//
+// Phase order. A parity wait cannot tell a phase from the one two later, so
+// every waiter observes every phase of the mbarriers it waits on, in order:
+// the ring holds one group's tiles per stage (tile t in stage t % NST, NST
+// even), so each stage's "full" and "empty" phases are one group's and one
+// copy thread's; each group waits for every block's "MMA done" in block
+// order (block t - 3, the other group's, before forming block t; its own
+// block t - 2 for the read-out); the MMA warp takes every "A full" and
+// "D free" phase in order.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -65,7 +77,8 @@ constexpr int TC_THREADS = TC_FEAT_THREADS + 64;
 constexpr int TC_M = 128;         // keys per MMA block (= rows per ring tile)
 constexpr int TC_N = 16;          // coefficient columns: hi and lo of up to eight heads
 constexpr int TC_HEADS = TC_N / 2;
-constexpr int TC_TMEM_COLS = 32;  // two accumulators of 16 columns
+constexpr int TC_NBUF = 3;       // operand buffers and accumulators, used by block index mod 3
+constexpr int TC_TMEM_COLS = 64;  // three accumulators of 16 columns (allocations are powers of two)
 constexpr int TC_ROWS_PER_CTA = 16384;
 constexpr uint32_t TC_IDESC = f16_idesc(TC_M, TC_N);
 
@@ -79,7 +92,7 @@ struct TcGeo {
   static constexpr int ROW_BYTES = D * 2;
   static constexpr int TILE_ROWS = TC_M;
   static constexpr int TILE_BYTES = TILE_ROWS * ROW_BYTES;
-  static constexpr int NST = TILE_BYTES >= 32768 ? 3 : 4;  // ring stages
+  static constexpr int NST = 65536 / TILE_BYTES;         // ring stages (64 KB)
   static constexpr int RPW = TILE_ROWS / TC_GROUP_WARPS;  // rows per warp per tile
   static constexpr int STEPS = RPW / KPW;                 // keys per lane per tile
   static constexpr int KF = 3 * F;                        // features per key
@@ -89,16 +102,16 @@ struct TcGeo {
   static constexpr int B_ATOM = TC_N * 128;
   static constexpr int A_BYTES = KATOMS * A_ATOM;
   static constexpr int B_BYTES = KATOMS * B_ATOM;
-  static_assert(KF % 16 == 0 && STEPS >= 1 && RPW % KPW == 0, "geometry");
+  static_assert(KF % 16 == 0 && STEPS >= 1 && RPW % KPW == 0 && NST >= 2, "geometry");
 };
 
 template <int NST>
 struct TcCtrl {
   uint64_t full[NST];    // ring stage holds its tile (bulk copy completion)
   uint64_t empty[NST];   // a group is done with the stage's tile
-  uint64_t a_full[2];    // per group: the features of its block are written
-  uint64_t mma_done[2];  // per group: its block's MMAs have completed
-  uint64_t d_free[2];    // per group: its accumulator was read out
+  uint64_t a_full[TC_NBUF];    // per buffer: the features of its block are written
+  uint64_t mma_done[TC_NBUF];  // per buffer: its block's MMAs have completed
+  uint64_t d_free[TC_NBUF];    // per buffer: its accumulator was read out
   uint64_t final_done;   // every MMA issued has completed (exit)
   int failed;            // a wait timed out
   int issued;            // tiles whose copies were issued
@@ -115,16 +128,16 @@ struct TcCtrl {
 template <int D>
 struct TcLayout {
   using G = TcGeo<D>;
-  static constexpr size_t OFF_A = 0;  // one buffer per group
-  static constexpr size_t OFF_B = OFF_A + 2 * static_cast<size_t>(G::A_BYTES);
+  static constexpr size_t OFF_A = 0;  // TC_NBUF operand buffers
+  static constexpr size_t OFF_B = OFF_A + TC_NBUF * static_cast<size_t>(G::A_BYTES);
   static constexpr size_t OFF_RING = OFF_B + G::B_BYTES;
   static constexpr size_t OFF_CTRL = OFF_RING + static_cast<size_t>(G::NST) * G::TILE_BYTES;
   static constexpr size_t BYTES = OFF_CTRL + (sizeof(TcCtrl<G::NST>) + 15) / 16 * 16;
   static constexpr size_t SMEM = BYTES + 1024;  // room to align the operands to 1024 bytes
   static_assert(OFF_B % 1024 == 0 && OFF_RING % 1024 == 0, "operand alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  // statistics scratch [feature thread][4][3] doubles, in A once the last MMA is done
-  static_assert(TC_FEAT_THREADS * 4 * 3 * sizeof(double) <= 2 * static_cast<size_t>(G::A_BYTES), "scratch fits");
+  // statistics scratch [head][2][256] doubles, in A once the last MMA is done
+  static_assert(TC_HEADS * 2 * 256 * sizeof(double) <= TC_NBUF * static_cast<size_t>(G::A_BYTES), "scratch fits");
   // coefficient scratch [TC_HEADS][F][3] floats, in A before the first block
   static_assert(TC_HEADS * G::F * 3 * sizeof(float) <= static_cast<size_t>(G::A_BYTES), "coefficients fit");
 };
@@ -180,7 +193,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&ctrl.full[st], 1);
       mbar_init(&ctrl.empty[st], TC_GROUP_THREADS);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < TC_NBUF; ++b) {
       mbar_init(&ctrl.a_full[b], TC_GROUP_THREADS);
       mbar_init(&ctrl.mma_done[b], 1);
       mbar_init(&ctrl.d_free[b], TC_GROUP_THREADS);
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       for (int u = 0; u < ntiles; ++u) {
         const int st = u % NST;
-        if (u >= NST && !mbar_wait_backoff(&ctrl.empty[st], static_cast<uint32_t>((u / NST - 1) & 1))) {
+        if (u >= NST && !mbar_wait_sleep(&ctrl.empty[st], static_cast<uint32_t>((u / NST - 1) & 1))) {
           fail();
           break;
         }
@@ -319,19 +332,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ---- the MMA warp: the whole warp follows the blocks (its values stay
     // warp-uniform); one elected lane issues every block's MMAs -------------
     const uint64_t b_desc0 = sw128_desc(smem_addr(sB));
-    const uint64_t a_desc_0 = sw128_desc(smem_addr(sA)), a_desc_1 = sw128_desc(smem_addr(sA + G::A_BYTES));
+    const uint64_t a_desc0 = sw128_desc(smem_addr(sA));
     for (int t = 0; t < ntiles; ++t) {
-      const int gi = t & 1;
-      bool ok = mbar_wait_backoff(&ctrl.a_full[gi], static_cast<uint32_t>((t >> 1) & 1));
-      if (ok && t >= 2) ok = mbar_wait_backoff(&ctrl.d_free[gi], static_cast<uint32_t>(((t - 2) >> 1) & 1));
+      // block t uses operand buffer and accumulator bi; accumulator bi is
+      // free once block t - 3 was read out
+      const int bi = t % TC_NBUF;
+      bool ok = mbar_wait_backoff(&ctrl.a_full[bi], static_cast<uint32_t>((t / TC_NBUF) & 1));
+      if (ok && t >= TC_NBUF)
+        ok = mbar_wait_backoff(&ctrl.d_free[bi], static_cast<uint32_t>((t / TC_NBUF - 1) & 1));
       ok = __all_sync(FULL_MASK, ok) && !failed();
       if (!ok) {
         if (lane == 0) fail();
         break;
       }
       tc_fence_after();
-      const uint32_t d = tmem + static_cast<uint32_t>(gi * TC_N);
-      const uint64_t a_desc = gi ? a_desc_1 : a_desc_0;
+      const uint32_t d = tmem + static_cast<uint32_t>(bi * TC_N);
+      const uint64_t a_desc = a_desc0 + ((static_cast<uint64_t>(bi) * G::A_BYTES) >> 4);
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < G::KSTEPS; ++k) {
@@ -340,7 +356,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint64_t off_b = ((k / 4) * G::B_ATOM + (k % 4) * 32) >> 4;
           umma_f16(d, a_desc + off_a, b_desc0 + off_b, TC_IDESC, k > 0);
         }
-        umma_commit(&ctrl.mma_done[gi]);
+        umma_commit(&ctrl.mma_done[bi]);
       }
       __syncwarp();
       mma_issued = t + 1;
@@ -385,7 +401,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         aoff[j][sec] = static_cast<uint32_t>((k / 64) * G::A_ATOM) + sw128_offset(rbase + j * KPW, (k % 64) * 2);
       }
     }
-    unsigned char* a = sA + gi * G::A_BYTES;
 
     float* out = p.scores_g + (s * p.group + p.head0) * static_cast<int64_t>(p.n_cap);
     const int32_t* pos = EXPLICIT_POS ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
@@ -401,11 +416,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
     // the scores of block b (this group's) from its accumulator
     auto readout = [&](int b) {
-      if (!warp_wait(&ctrl.mma_done[gi], b >> 1)) return false;
+      const int bi = b % TC_NBUF;
+      if (!warp_wait(&ctrl.mma_done[bi], b / TC_NBUF)) return false;
       tc_fence_after();
       if (eg < gh) {  // warp-uniform
         uint32_t d[8];
-        tmem_ld8(tmem + (static_cast<uint32_t>(eq * 32) << 16) + static_cast<uint32_t>(gi * TC_N + 2 * eg), d);
+        __syncwarp();  // the load is a whole-warp (aligned) instruction
+        tmem_ld8(tmem + (static_cast<uint32_t>(eq * 32) << 16) + static_cast<uint32_t>(bi * TC_N + 2 * eg), d);
         tmem_wait_ld();
         const int row = c0 + b * TC_M + eq * 32 + lane;
         if (row < c1) {
@@ -425,17 +442,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&ctrl.d_free[gi]);
+      mbar_arrive(&ctrl.d_free[bi]);
       return true;
     };
 
     int last = -1;  // this group's last block
     for (int t = gi; t < ntiles; t += 2) {
       if (!warp_wait(&ctrl.full[t % NST], t / NST)) break;
-      // block t - 2 (this buffer's previous block): its MMAs are done once
-      // its accumulator can be read; then the buffer is free for block t
-      if (t >= 2 && !readout(t - 2)) break;
+      // the lane's chunks of the tile go to registers, and the stage is
+      // handed back to the copy warp before any arithmetic
       const unsigned char* tile = ring + (t % NST) * G::TILE_BYTES;
+      uint4 raw[STEPS];
+#pragma unroll
+      for (int j = 0; j < STEPS; ++j) raw[j] = lds_chunk<T, D, STYLE>(tile + (rbase + j * KPW) * ROW_BYTES, c);
+      mbar_arrive(&ctrl.empty[t % NST]);
+      // operand buffer t % 3 held block t - 3 (the other group's): free once
+      // that block's MMAs are done
+      if (t >= TC_NBUF && !warp_wait(&ctrl.mma_done[t % TC_NBUF], t / TC_NBUF - 1)) break;
+      unsigned char* a = sA + (t % TC_NBUF) * G::A_BYTES;
       int pp[STEPS];
       if (EXPLICIT_POS) {
 #pragma unroll
@@ -448,10 +472,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int j = 0; j < STEPS; ++j) {
         // rows past the run's end hold stale bytes: their accumulator rows
         // are never read out
-        const int rt = rbase + j * KPW;
-        const uint4 raw = lds_chunk<T, D, STYLE>(tile + rt * ROW_BYTES, c);
         float re[BPT], im[BPT];
-        decode_chunk<T, STYLE>(raw, re, im);
+        decode_chunk<T, STYLE>(raw[j], re, im);
         uint32_t hz[NP], hn[NP], hm[NP];
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -486,9 +508,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         *reinterpret_cast<uint2*>(a + aoff[j][1]) = make_uint2(hn[0], hn[1]);
         *reinterpret_cast<uint2*>(a + aoff[j][2]) = make_uint2(hm[0], hm[1]);
       }
-      fence_proxy_async_smem();           // the features are read by the tensor cores
-      mbar_arrive(&ctrl.empty[t % NST]);  // the tile's bytes are no longer needed
-      mbar_arrive(&ctrl.a_full[gi]);
+      fence_proxy_async_smem();  // the features are read by the tensor cores
+      mbar_arrive(&ctrl.a_full[t % TC_NBUF]);
+      // the group's previous block, whose MMAs ran while these features
+      // were formed
+      if (t >= 2 && !readout(t - 2)) break;
       last = t;
       if (failed()) break;
       if (PM == POS_SLOT) {
@@ -530,38 +554,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 
   // ---- statistics partials of this CTA, per head, in fp64 -------------------
-  double* spart = reinterpret_cast<double*>(sA);  // [feature thread][4][3]
+  // Head g was read out by the 256 threads of both groups' warps with
+  // gw / 4 == g / hpw, slot g % hpw; each turns its shifted sums into plain
+  // ones, and a tree of fixed shape adds the 256 (the fp64 pipe is slow, so
+  // no long serial chain). Every row of the run was read once per head: the
+  // count is c1 - c0.
+  double* spart = reinterpret_cast<double*>(sA);  // [head][sum, sum of squares][256]
   if (tid < TC_FEAT_THREADS) {
+    const int gw = warp % TC_GROUP_WARPS, half = gw >> 2;
+    const int ci = ((warp / TC_GROUP_WARPS) * 4 + (gw & 3)) * 32 + lane;
     const double dn = cnt;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      const double dsh = sh[h], ds1 = s1[h];
-      double* e = spart + (tid * 4 + h) * 3;
-      e[0] = dn * dsh + ds1;                                                  // sum
-      e[1] = dn * dsh * dsh + 2.0 * dsh * ds1 + static_cast<double>(s2[h]);  // sum of squares
-      e[2] = dn;
+      const int g = half * hpw + h;
+      if (h < hpw && g < gh) {
+        const double dsh = sh[h], ds1 = s1[h];
+        spart[(g * 2 + 0) * 256 + ci] = dn * dsh + ds1;
+        spart[(g * 2 + 1) * 256 + ci] = dn * dsh * dsh + 2.0 * dsh * ds1 + static_cast<double>(s2[h]);
+      }
     }
   }
   __syncthreads();
-  if (tid < gh) {
-    // head g lives in the warps of both groups with gw / 4 == g / hpw, slot
-    // g % hpw; fixed order
-    const int half = tid / hpw, hsel = tid % hpw;
-    double a0 = 0.0, a1 = 0.0, a2 = 0.0;
-    for (int g2 = 0; g2 < 2; ++g2) {
-      for (int w = half * 4; w < half * 4 + 4; ++w) {
-        for (int l = 0; l < 32; ++l) {
-          const int u = (g2 * TC_GROUP_WARPS + w) * 32 + l;
-          const double* e = spart + (u * 4 + hsel) * 3;
-          a0 += e[0];
-          a1 += e[1];
-          a2 += e[2];
-        }
-      }
+  for (int stride = 128; stride >= 1; stride >>= 1) {
+    for (int i = tid; i < gh * 2 * stride; i += TC_THREADS) {
+      const int gv = i / stride, k = i % stride;
+      spart[gv * 256 + k] += spart[gv * 256 + k + stride];
     }
-    my_part[3 * tid + 0] = a0;
-    my_part[3 * tid + 1] = a1;
-    my_part[3 * tid + 2] = a2;
+    __syncthreads();
+  }
+  if (tid < gh) {
+    my_part[3 * tid + 0] = spart[(tid * 2 + 0) * 256];
+    my_part[3 * tid + 1] = spart[(tid * 2 + 1) * 256];
+    my_part[3 * tid + 2] = static_cast<double>(c1 - c0);
   }
 }
 
