@@ -22,8 +22,8 @@
 //
 // Statistics: each lane that owns a (key, head) sum also accumulates that
 // head's sum and sum of squares, shifted by the first value it saw so that
-// fp32 only sees deviations; the CTA combines the lanes in fp64 in a fixed
-// order into one partial per (CTA, head), and heads_stats_kernel adds the
+// fp32 only sees deviations; the CTA combines the lanes in fp64 by a tree of
+// fixed shape into one partial per (CTA, head), and heads_stats_kernel adds the
 // partials of a slice in order. The results do not depend on scheduling.
 #include <cuda_runtime.h>
 
@@ -35,8 +35,8 @@
 namespace tri {
 namespace {
 
-constexpr size_t HEADS_STATS_OFF = SCORE_SMEM;  // 16-byte aligned
-constexpr size_t HEADS_JUMP_OFF = HEADS_STATS_OFF + SCORE_THREADS * (3 * sizeof(double) + sizeof(int));
+constexpr size_t HEADS_BAD_OFF = SCORE_SMEM;  // the paged check's first bad block (16-byte slot)
+constexpr size_t HEADS_JUMP_OFF = HEADS_BAD_OFF + 16;
 constexpr size_t HEADS_SMEM = HEADS_JUMP_OFF + MAX_BANDS / 2 * sizeof(float4);
 
 // Sums a[0..NU) over the TPK lanes of a key group. Each lane ends with RPL =
@@ -80,11 +80,11 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
   constexpr int NU = GHP * HS;
   constexpr int RPL = (NU >= TPK) ? NU / TPK : 1;
   static_assert(STEPS % HS == 0, "steps per reduction");
+  static_assert(GH * 3 * SCORE_THREADS * sizeof(double) <= RING_BYTES, "statistics rows fit in the ring");
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   RingCtrl& rc = *reinterpret_cast<RingCtrl*>(smem + RING_BYTES);
-  double* spart = reinterpret_cast<double*>(smem + HEADS_STATS_OFF);  // [threads][3]
-  int* shead = reinterpret_cast<int*>(spart + 3 * SCORE_THREADS);     // [threads]
+  int* sbad = reinterpret_cast<int*>(smem + HEADS_BAD_OFF);
   // per band pair: the tile-to-tile rotation (re0, re1, im0, im1)
   float4* sjump = reinterpret_cast<float4*>(smem + HEADS_JUMP_OFF);
 
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
   const unsigned char* kbase = static_cast<const unsigned char*>(p.k);
   const int64_t sbase = p.rows.slice_base(s);
   const int32_t* trow = p.rows.seq_table(s);
-  if (!p.rows.blocks_ok(trow, c0, c1, shead)) {  // uniform over the CTA; shead is free until the end
+  if (!p.rows.blocks_ok(trow, c0, c1, sbad)) {  // uniform over the CTA
     if (threadIdx.x == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
     if (threadIdx.x < 3 * GH) my_part[threadIdx.x] = 0.0;
     return;
@@ -304,27 +304,33 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2)
   ring_drain(rc, p.dev_status);
 
   // ---- statistics partials of this CTA, per head, in fp64 -------------------
+  // Thread u's plain sums go to column u of its head's three rows (zeros in
+  // the other heads' rows), and a tree of fixed shape adds each row's
+  // columns: no long serial chain on the slow fp64 pipe. The drained ring
+  // holds the rows.
+  __syncthreads();
+  double* sx = reinterpret_cast<double*>(ring);  // [GH][3][SCORE_THREADS]
   {
     const double dn = cnt, dsh = sh, ds1 = s1;
-    spart[3 * threadIdx.x + 0] = dn * dsh + ds1;                                        // sum
-    spart[3 * threadIdx.x + 1] = dn * dsh * dsh + 2.0 * dsh * ds1 + static_cast<double>(s2);  // sum of squares
-    spart[3 * threadIdx.x + 2] = dn;
-    shead[threadIdx.x] = lane_head;
+    const double e0 = dn * dsh + ds1;                                        // sum
+    const double e1 = dn * dsh * dsh + 2.0 * dsh * ds1 + static_cast<double>(s2);  // sum of squares
+#pragma unroll
+    for (int g = 0; g < GH; ++g) {
+      const bool mine = g == lane_head;
+      sx[(g * 3 + 0) * SCORE_THREADS + threadIdx.x] = mine ? e0 : 0.0;
+      sx[(g * 3 + 1) * SCORE_THREADS + threadIdx.x] = mine ? e1 : 0.0;
+      sx[(g * 3 + 2) * SCORE_THREADS + threadIdx.x] = mine ? dn : 0.0;
+    }
   }
   __syncthreads();
-  if (threadIdx.x < GH) {
-    double a0 = 0.0, a1 = 0.0, a2 = 0.0;
-    for (int u = 0; u < SCORE_THREADS; ++u) {
-      if (shead[u] == static_cast<int>(threadIdx.x)) {
-        a0 += spart[3 * u + 0];
-        a1 += spart[3 * u + 1];
-        a2 += spart[3 * u + 2];
-      }
+  for (int stride = SCORE_THREADS / 2; stride >= 1; stride >>= 1) {
+    for (int i = threadIdx.x; i < GH * 3 * stride; i += SCORE_THREADS) {
+      const int r = i / stride, k = i % stride;
+      sx[r * SCORE_THREADS + k] += sx[r * SCORE_THREADS + k + stride];
     }
-    my_part[3 * threadIdx.x + 0] = a0;
-    my_part[3 * threadIdx.x + 1] = a1;
-    my_part[3 * threadIdx.x + 2] = a2;
+    __syncthreads();
   }
+  if (threadIdx.x < 3 * GH) my_part[threadIdx.x] = sx[threadIdx.x * SCORE_THREADS];
 }
 
 // One thread per (slice, head): the partials of the slice's CTAs in order.

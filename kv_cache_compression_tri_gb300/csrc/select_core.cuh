@@ -53,7 +53,7 @@ constexpr int BM_WORDS = BM_SLOTS / 32;
 constexpr int LCAP = 4096;           // short-list capacity
 constexpr int SPT = 8;               // sampled scores per thread
 constexpr int NSAMPLE = NT * SPT;    // 2048
-constexpr double SAMPLE_SD = 4.5;    // half-width of the sampled window, in sd
+constexpr float SAMPLE_SD = 4.5f;    // half-width of the sampled window, in sd
 constexpr double DRAW_SD = 8.0;      // half-width of the uniform-draw window, in sd
 
 struct SSmem {
@@ -248,10 +248,11 @@ __device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const K
   }
   block_minmax(sm, kmin, kmax);
   // sample ranks (1 = largest) that bracket the need-th largest candidate
-  const double rho = static_cast<double>(need) / m;
-  const double rs = rho * NSAMPLE, sd = sqrt(NSAMPLE * rho * (1.0 - rho));
-  const int ra = static_cast<int>(floor(rs - SAMPLE_SD * sd - 1.0));
-  const int rb = static_cast<int>(ceil(rs + SAMPLE_SD * sd + 1.0));
+  // (fp32: the window only has to be about right, and the fp64 pipe is slow)
+  const float rho = static_cast<float>(need) / static_cast<float>(m);
+  const float rs = rho * NSAMPLE, sd = sqrtf(NSAMPLE * rho * (1.0f - rho));
+  const int ra = static_cast<int>(floorf(rs - SAMPLE_SD * sd - 1.0f));
+  const int rb = static_cast<int>(ceilf(rs + SAMPLE_SD * sd + 1.0f));
   Radix A, B;
   const bool want_a = ra >= 1, want_b = rb <= NSAMPLE;
   A.start(kmin, kmax, static_cast<unsigned>(max(ra, 1)));
