@@ -26,7 +26,10 @@
 // z-score selection reports TRI_DEV_NAN_SCORE.
 //
 // CTA: one per SM, a run of up to 16384 rows of one slice, with two groups
-// of eight feature warps, an MMA warp and a copy warp. The copy warp streams
+// of four feature warps, an MMA warp and a copy warp (ten warps: at most
+// three share a scheduler, so a thread may hold up to 168 registers and each
+// feature warp forms 32 keys of a block with the loads of all of them in
+// flight). The copy warp streams
 // key tiles of 128 rows into a 64 KB ring (bulk async copies completing on
 // "full" mbarriers; a stage is refilled once its "empty" mbarrier says the
 // tile was taken). Each tile is one MMA block; the two groups take
@@ -39,10 +42,10 @@
 // arrives on "A full"; the MMA warp issues the block's MMAs into accumulator
 // t % 3 and commits them to "MMA done"; the group then reads out its
 // previous block t - 2, whose MMAs ran while it formed block t -- each warp
-// 32 keys (its quarter of the tensor-memory lanes) and half of the heads --
+// 32 keys (its quarter of the tensor-memory lanes) and every head --
 // stores the scores, adds them to the heads' statistics (sum and sum of
-// squares shifted by the thread's first value, folded in fp64 in a fixed
-// order into one partial per CTA and head, as score_heads.cu does) and
+// squares shifted by the thread's first value, folded in fp64 by a tree of
+// fixed shape into one partial per CTA and head) and
 // arrives on "D free", which the MMA warp waits for before block t + 1
 // overwrites that accumulator. No group waits for its own block's MMAs, no
 // CTA barrier in the loop; every wait is bounded.
@@ -67,7 +70,7 @@
 namespace tri {
 namespace {
 
-constexpr int TC_GROUP_WARPS = 8;                        // feature warps per group
+constexpr int TC_GROUP_WARPS = 4;                        // feature warps per group
 constexpr int TC_GROUP_THREADS = TC_GROUP_WARPS * 32;
 constexpr int TC_FEAT_WARPS = 2 * TC_GROUP_WARPS;
 constexpr int TC_FEAT_THREADS = TC_FEAT_WARPS * 32;
@@ -77,6 +80,8 @@ constexpr int TC_THREADS = TC_FEAT_THREADS + 64;
 constexpr int TC_M = 128;         // keys per MMA block (= rows per ring tile)
 constexpr int TC_N = 16;          // coefficient columns: hi and lo of up to eight heads
 constexpr int TC_HEADS = TC_N / 2;
+constexpr int TC_HSPLIT = TC_GROUP_WARPS / 4;          // warps sharing a quarter of the lanes
+constexpr int TC_HPW = TC_HEADS / TC_HSPLIT;           // heads one read-out warp may hold
 constexpr int TC_NBUF = 3;       // operand buffers and accumulators, used by block index mod 3
 constexpr int TC_TMEM_COLS = 64;  // three accumulators of 16 columns (allocations are powers of two)
 constexpr int TC_ROWS_PER_CTA = 16384;
@@ -324,10 +329,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     feat_sync();  // and A is free again
   }
 
-  float sh[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+  float sh[TC_HPW] = {}, s1[TC_HPW] = {}, s2[TC_HPW] = {};
   int cnt = 0;
   int mma_issued = 0;  // MMA thread: blocks issued
-  const int hpw = (gh + 1) / 2;  // heads per read-out warp
+  const int hpw = (gh + TC_HSPLIT - 1) / TC_HSPLIT;  // heads per read-out warp
   if (warp == TC_MMA_WARP) {
     // ---- the MMA warp: the whole warp follows the blocks (its values stay
     // warp-uniform); one elected lane issues every block's MMAs -------------
@@ -420,14 +425,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (!warp_wait(&ctrl.mma_done[bi], b / TC_NBUF)) return false;
       tc_fence_after();
       if (eg < gh) {  // warp-uniform
-        uint32_t d[8];
+        uint32_t d[2 * TC_HPW];
         __syncwarp();  // the load is a whole-warp (aligned) instruction
-        tmem_ld8(tmem + (static_cast<uint32_t>(eq * 32) << 16) + static_cast<uint32_t>(bi * TC_N + 2 * eg), d);
+        const uint32_t ta = tmem + (static_cast<uint32_t>(eq * 32) << 16) + static_cast<uint32_t>(bi * TC_N + 2 * eg);
+        tmem_ld8(ta, *reinterpret_cast<uint32_t(*)[8]>(&d[0]));
+        if constexpr (TC_HPW > 4) {
+          if (hpw > 4) tmem_ld8(ta + 8u, *reinterpret_cast<uint32_t(*)[8]>(&d[8]));
+        }
         tmem_wait_ld();
         const int row = c0 + b * TC_M + eq * 32 + lane;
         if (row < c1) {
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
+          for (int h = 0; h < TC_HPW; ++h) {
             const int g = eg + h;
             if (h < hpw && g < gh) {
               const float v = (__uint_as_float(d[2 * h]) + __uint_as_float(d[2 * h + 1])) * ctrl.unscale[g];
@@ -565,7 +574,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int ci = ((warp / TC_GROUP_WARPS) * 4 + (gw & 3)) * 32 + lane;
     const double dn = cnt;
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
+    for (int h = 0; h < TC_HPW; ++h) {
       const int g = half * hpw + h;
       if (h < hpw && g < gh) {
         const double dsh = sh[h], ds1 = s1[h];
