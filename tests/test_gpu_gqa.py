@@ -134,6 +134,16 @@ def test_gqa_group_sizes(group):
     _heads_case(w, seed=group)
 
 
+@pytest.mark.parametrize("group", [4, 8])
+def test_gqa_bf16_d128_runs_of_one_to_three_blocks(group):
+    # 300-row caches: a CTA's run is one to three 128-row blocks (the second
+    # group of feature warps idle, or the third operand buffer unused), with
+    # ragged row counts 0, 1 and in between
+    w = synth.scaled(LAYER, group=group, n_kv_heads=2, n_layers=3, n_cap=300, n_valid=300, n_cal=256,
+                     n_prompt=8, n_recent=8, budget=64)
+    _heads_case(w, ragged=True, seed=10 + group)
+
+
 def test_gqa_bf16_d64_and_fp32_d128():
     w1 = synth.scaled(TINY, dtype=torch.bfloat16, n_seq=2, n_layers=2, n_kv_heads=2, group=4, n_cap=1000,
                       n_valid=1000, n_cal=512, n_prompt=16, n_recent=16, budget=250)
