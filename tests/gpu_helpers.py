@@ -1,9 +1,9 @@
 """Shared pieces of the GPU parity tests: run the oracle on chosen slices of
 the same inputs the CUDA path consumed, and the comparison rules.
 
-Tolerances (the score tolerance 1e-3 relative comes from the benchmark spec
-of this build; the bound M(i) = sum_f E|q_f| |k_f| >= |S~(i)| makes it well
-posed for scores near zero):
+Tolerances (scores to 1e-3 relative, measured against the bound
+M(i) = sum_f E|q_f| |k_f| >= |S~(i)|, which keeps the test well posed for
+scores near zero):
   scores        |s_gpu - s_ref| <= 1e-3 * M(i)
   selection     the GPU keep set G is valid when |G| = B, protected rows are
                 in it, it is ascending, and no kept candidate i and dropped
