@@ -195,3 +195,68 @@ def test_planted_missing_operand_buffer_wait_is_caught():
         except Violation as e:
             caught.append(str(e))
     assert caught and any("operand buffer" in c for c in caught)
+
+
+def run_shared_ring(ntiles, nst, nw, rng):
+    """The CUDA-core score kernels' ring (score_common.cuh): nw warps each
+    take every tile in order (waiting on the stage's full barrier by parity),
+    count themselves done on the stage, and the last one of tile t refills
+    the stage with tile t + nst. Warps drift apart by up to the ring depth."""
+    full = [Barrier(f"full[{s}]", 1) for s in range(nst)]
+    consumed = [0] * nst
+    stage = [None] * nst
+    pending = []
+
+    def wait(bar, j):
+        while True:
+            k = bar.phase
+            if not (k == j or k == j + 1):
+                raise Violation(f"{bar.name}: wait for phase {j} while phase {k} is in progress")
+            if k == j + 1:
+                return
+            yield
+
+    def issue(u):
+        stage[u % nst] = None
+        pending.append(u)
+
+    def warp(w):
+        for t in range(ntiles):
+            st = t % nst
+            yield from wait(full[st], t // nst)
+            if stage[st] != t:
+                raise Violation(f"warp {w} read stage {st} for tile {t}, it holds {stage[st]}")
+            yield
+            if stage[st] != t:
+                raise Violation(f"stage {st} refilled while warp {w} read tile {t}")
+            consumed[st] += 1
+            if consumed[st] == nw:
+                consumed[st] = 0
+                if t + nst < ntiles:
+                    issue(t + nst)
+
+    for u in range(min(nst, ntiles)):
+        issue(u)
+    live = [warp(w) for w in range(nw)]
+    steps = 0
+    while live or pending:
+        steps += 1
+        if steps > 200000:
+            raise Violation("no progress (deadlock)")
+        if pending and (not live or rng.random() < 0.3):
+            u = pending.pop(rng.randrange(len(pending)))
+            stage[u % nst] = u
+            full[u % nst].arrive()
+            continue
+        a = rng.choice(live)
+        try:
+            next(a)
+        except StopIteration:
+            live.remove(a)
+
+
+def test_shared_ring_with_drifting_warps_holds():
+    rng = random.Random(7)
+    for ntiles in (1, 3, 4, 9, 17):
+        for _ in range(200):
+            run_shared_ring(ntiles, nst=4, nw=8, rng=rng)
