@@ -386,6 +386,18 @@ tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_pro
  * ------------------------------------------------------------------------ */
 tri_status tri_paged_blocks_used(const tri_kv* kv, int32_t* blocks_used, tri_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * tri_selftest_wait_timeout -- a check of the failure path every kernel
+ * shares: one thread waits on an mbarrier that nothing arrives on for
+ * limit_ns nanoseconds of the GPU's global timer (1000 <= limit_ns <=
+ * 1000000000), then sets *dev_status to TRI_DEV_TIMEOUT (first error wins)
+ * and returns -- what each bounded in-kernel wait does after about 2 s.
+ * The context stays usable. dev_status: device int32, required, 4-byte
+ * aligned. Stream-ordered; TRI_ERR_INVALID_ARG for a null status word or a
+ * limit out of range (nothing is launched then).
+ * ------------------------------------------------------------------------ */
+tri_status tri_selftest_wait_timeout(int32_t* dev_status, uint64_t limit_ns, tri_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

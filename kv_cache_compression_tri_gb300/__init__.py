@@ -122,6 +122,8 @@ def load_library():
         lib.rand_evict_compact.restype = ctypes.c_int
         lib.tri_paged_blocks_used.argtypes = [kvp, vp, vp]
         lib.tri_paged_blocks_used.restype = ctypes.c_int
+        lib.tri_selftest_wait_timeout.argtypes = [vp, u64, vp]
+        lib.tri_selftest_wait_timeout.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -270,6 +272,17 @@ def paged_blocks_used(kv: PagedKVCache, out: torch.Tensor, stream=None) -> torch
     kvs = kv._abi()
     _check("tri_paged_blocks_used", lib.tri_paged_blocks_used(ctypes.byref(kvs), out.data_ptr(), _stream(stream)))
     return out
+
+
+def selftest_wait_timeout(status: torch.Tensor, limit_ns: int, stream=None) -> torch.Tensor:
+    """The kernels' failure path (tri_selftest_wait_timeout): a bounded wait
+    on an mbarrier nothing arrives on runs out after limit_ns and sets
+    status (device int32 [1]) to DEV_TIMEOUT."""
+    lib = load_library()
+    assert status.dtype == torch.int32 and status.is_cuda and status.numel() >= 1
+    _check("tri_selftest_wait_timeout", lib.tri_selftest_wait_timeout(status.data_ptr(), int(limit_ns),
+                                                                      _stream(stream)))
+    return status
 
 
 def calibrate_workspace_bytes(n_layers: int, n_q_heads: int, group: int, head_dim: int,

@@ -574,4 +574,10 @@ tri_status tri_paged_blocks_used(const tri_kv* kv, int32_t* blocks_used, tri_str
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 
+tri_status tri_selftest_wait_timeout(int32_t* dev_status, uint64_t limit_ns, tri_stream_t stream) {
+  if (!dev_status || !aligned(dev_status, 4) || limit_ns < 1000u || limit_ns > 1000000000u) return TRI_ERR_INVALID_ARG;
+  const cudaError_t e = launch_wait_timeout_selftest(dev_status, limit_ns, stream);
+  return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -148,13 +148,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Wait for phase `parity` of `bar`; gives up after ~2 s of wall clock so a
 // lost completion can never hang the GPU (the caller reports TRI_DEV_TIMEOUT).
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_limit(bar, parity, WAIT_LIMIT_NS);
 }
 
 // sqrt of a non-negative fp32 (hardware approximation; exact at 0). The
@@ -370,6 +373,9 @@ cudaError_t launch_slice_stats(const float* scores, const int32_t* n_valid, floa
                                cudaStream_t st);
 cudaError_t launch_blocks_used(const RowMap& rows, const int32_t* n_valid, int32_t* blocks_used, int n_seq,
                                cudaStream_t st);
+// Self-test of the bounded waits: one thread waits on an mbarrier that
+// nothing arrives on, for at most limit_ns, and records TRI_DEV_TIMEOUT.
+cudaError_t launch_wait_timeout_selftest(int32_t* dev_status, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_select_union(const SelectParams& p, int n_groups, cudaStream_t st);
 cudaError_t launch_select_zmax(const SelectParams& p, int n_slices, cudaStream_t st);
 cudaError_t launch_rand_select(const SelectParams& p, int n_slices, cudaStream_t st);

@@ -197,3 +197,11 @@ def test_gqa_entry_points_reject_bad_args(lib):
 def test_paged_blocks_used_needs_a_paged_cache(lib):
     assert lib.tri_paged_blocks_used(ctypes.byref(_kv()), 0x50000, None) == INVALID
     assert lib.tri_paged_blocks_used(ctypes.byref(_kv(**PAGED)), None, None) == INVALID
+
+
+def test_wait_timeout_selftest_rejects_bad_args(lib):
+    f = lib.tri_selftest_wait_timeout
+    assert f(None, 1000000, None) == INVALID  # no status word
+    assert f(0x10002, 1000000, None) == INVALID  # misaligned status word
+    assert f(0x10000, 999, None) == INVALID  # limit below 1 us
+    assert f(0x10000, 1000000001, None) == INVALID  # limit above 1 s
