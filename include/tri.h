@@ -107,9 +107,9 @@ typedef struct {
   tri_dtype dtype;       /* element type of k and v                              */
   int32_t* dev_status;   /* device int32 status word (TRI_DEV_*), or NULL        */
   tri_key_layout key_layout; /* pre- or post-RoPE keys (0 = pre-RoPE)            */
-  /* Paged caches (block_table != NULL; [RA] section 6: the score is a pass
-   * "through vLLM's block tables", eviction rewrites the survivors into the
-   * request's blocks and frees the tail). k and v are then block pools, and
+  /* Paged caches (block_table != NULL; [RA] section 6: scoring walks the
+   * engine's block tables, and eviction moves the survivors to the front of
+   * the request's blocks and returns the unused tail). k and v are then block pools, and
    * logical row r of slice (seq, layer, head) is at element
    *   block_table[seq][r / block_size] * block_stride + layer * layer_stride
    *   + head * head_stride + (r % block_size) * head_dim
@@ -174,9 +174,11 @@ tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layer
  * allocates nothing.
  *   - Shapes whose scratch (tri_calibrate_workspace_bytes) exceeds the array
  *     return TRI_ERR_INVALID_ARG before anything is enqueued.
- *   - The first call on each device looks up the array's device address
- *     (once per device, with that device current); make that first call
- *     before any stream capture begins.
+ *   - Every call looks up the array's address in the current device's
+ *     context (a host-side query; it stays right after cudaDeviceReset and
+ *     under another context). The first call on a device may load the
+ *     library's device code there: make that first call before any stream
+ *     capture begins.
  *   - All calls share the one array, and each call fully rewrites the part it
  *     reads, so nothing carries over between calls; but calls whose kernels
  *     overlap on the GPU (e.g. on two streams without ordering) race on it.
@@ -381,7 +383,7 @@ tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_pro
  * tri_paged_blocks_used -- after a compaction of a paged cache: the blocks
  * each sequence still uses, ceil(max over its slices of n_valid / block_size);
  * table entries from there on hold no live row and can go back to the
- * caller's allocator ([RA] section 6: "free the tail"). blocks_used: device
+ * caller's allocator ([RA] section 6: unused tail blocks go back). blocks_used: device
  * [n_seq] int32. Requires a paged cache (block_table != NULL).
  * ------------------------------------------------------------------------ */
 tri_status tri_paged_blocks_used(const tri_kv* kv, int32_t* blocks_used, tri_stream_t stream);

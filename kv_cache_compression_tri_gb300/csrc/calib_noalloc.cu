@@ -10,13 +10,14 @@
 // array in this library's own device memory, so the call allocates nothing.
 //
 // The array is a file-scope __device__ variable. On the host its name is only
-// a stand-in, not a device address, so the host looks up the real address with
-// cudaGetSymbolAddress once per device (with that device current) and passes
-// it to the kernels. Every GPU that loads the library holds the array until
+// a stand-in, not a device address, so every call looks up the real address
+// with cudaGetSymbolAddress (a host-side query that allocates nothing) on the
+// current device and passes it to the kernels. Looking it up per call, rather
+// than caching it, keeps the address right after cudaDeviceReset (which loads
+// the module again, possibly elsewhere) and under a different driver context
+// of the same device. Every GPU that loads the library holds the array until
 // the process exits.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "tri_internal.cuh"
 
@@ -30,28 +31,12 @@ static_assert(NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
 
 static __device__ __align__(256) float g_calib_scratch[NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
-constexpr int MAX_DEVICES = 64;
-std::mutex g_mu;
-float* g_scratch_ptr[MAX_DEVICES] = {};
-
-// Device address of the scratch array on the current device (looked up once
-// per device), or nullptr with *err set.
+// Device address of the scratch array in the current device's context, or
+// nullptr with *err set.
 float* scratch_for_current_device(cudaError_t* err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= MAX_DEVICES) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_calib_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  return g_scratch_ptr[dev];
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_calib_scratch);
+  return *err == cudaSuccess ? static_cast<float*>(p) : nullptr;
 }
 
 }  // namespace

@@ -39,6 +39,11 @@ Parity status of each function (what pins it, all in ``tests/test_oracle_*``):
   zscore_max         -- a hand-worked two-head example in closed form,
                         invariance under a positive affine map of any head,
                         unit variance of every z-scored head, constant heads.
+  score_bound        -- hand-entered values for both band pairings;
+                        |score_series| <= M (weighted norm term) and
+                        0 <= score <= 2M (unweighted) on calibrated random
+                        cases; equality for a zero query centre and for an
+                        aligned concentrated band (tests/test_oracle_bound.py).
 """
 from __future__ import annotations
 
