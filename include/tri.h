@@ -295,12 +295,15 @@ tri_status rand_evict_compact(const tri_kv* kv, uint64_t seed, uint32_t round, t
 /* ------------------------------------------------------------------------
  * tri_compress -- one compression event: score + select + compact.
  * Exactly tri_score (rows [n_prompt, n_valid - n_recent)), tri_select_topk
- * and tri_compact_kv called in sequence with the same arguments (three
- * launches on the stream), with the scores kept in caller scratch.
+ * and tri_compact_kv called in sequence with the same arguments, with the
+ * scores kept in caller scratch. When a slice fits one CTA of the score
+ * kernel (n_cap at most 2048 rows of 256 B, 4096 of 128 B, ...: 32 tiles of
+ * 16 KB) one CTA scores, selects and compacts each slice in a single launch;
+ * otherwise the three kernels run in turn.
  * keep_idx: device [n_slices][budget], written as by tri_select_topk.
  * ws: device scratch of at least tri_compress_workspace_bytes(kv) bytes,
  * 16-byte aligned (the scores [n_slices][n_cap]; nothing in it needs to be
- * initialised or survives the call). kv->pos_out required.
+ * initialised; the candidates' scores are left there). kv->pos_out required.
  * ------------------------------------------------------------------------ */
 size_t tri_compress_workspace_bytes(const tri_kv* kv);
 tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_theta,

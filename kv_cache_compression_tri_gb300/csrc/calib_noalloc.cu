@@ -50,6 +50,7 @@ tri_status tri_calibrate_centers_noalloc(const void* q, tri_dtype dtype, int32_t
                                          int32_t n_q_heads, int32_t group, int32_t head_dim,
                                          int64_t n_tok, tri_rope_style style, tri_centers out,
                                          tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (dtype != TRI_BF16 && dtype != TRI_F32) return TRI_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return TRI_ERR_UNSUPPORTED;
   if (style != TRI_ROPE_INTERLEAVED && style != TRI_ROPE_HALF) return TRI_ERR_INVALID_ARG;

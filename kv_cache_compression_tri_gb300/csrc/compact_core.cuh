@@ -39,8 +39,8 @@ namespace {
 constexpr int CT = 128;  // threads per CTA: warps 0-1 move K/V rows, warps 2-3 positions
 constexpr int CSTAGES = 3;
 constexpr int CTILE = 8192;
-constexpr size_t RING_BYTES = CSTAGES * CTILE;
-constexpr size_t COMPACT_SMEM = 2 * RING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
+constexpr size_t CRING_BYTES = CSTAGES * CTILE;
+constexpr size_t COMPACT_SMEM = 2 * CRING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
 constexpr int CTAB = 2048;  // paged: table entries cached in shared memory (more are read from global)
 constexpr int POS_PER_THREAD = 8;
 
@@ -260,8 +260,8 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   if (wid < 2) {
     // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
     if (first < n_keep)
-      move_rows<PAGED, RO>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, smem + wid * RING_BYTES,
-                reinterpret_cast<uint64_t*>(smem + 2 * RING_BYTES) + wid * CSTAGES, keep, first, n_keep,
+      move_rows<PAGED, RO>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, smem + wid * CRING_BYTES,
+                reinterpret_cast<uint64_t*>(smem + 2 * CRING_BYTES) + wid * CSTAGES, keep, first, n_keep,
                 p.row_bytes, lane, p.dev_status);
     return;
   }

@@ -138,6 +138,7 @@ tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layer
                                  int32_t n_q_heads, int32_t group, int32_t head_dim,
                                  int64_t n_tok, tri_rope_style style, tri_centers out,
                                  void* ws, size_t ws_bytes, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (dtype != TRI_BF16 && dtype != TRI_F32) return TRI_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return TRI_ERR_UNSUPPORTED;
   if (style != TRI_ROPE_INTERLEAVED && style != TRI_ROPE_HALF) return TRI_ERR_INVALID_ARG;
@@ -276,6 +277,7 @@ tri_status tri_score(const tri_kv* kv, const tri_centers* c, double rope_theta,
                      tri_rope_style style, tri_norm_mode norm_mode, const int32_t* offsets,
                      int32_t n_offsets, const int64_t* p_cur, int32_t n_prompt,
                      int32_t n_recent, float* scores, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   ScoreParams p;
   const tri_status st = prepare_score(kv, c, rope_theta, style, norm_mode, offsets, n_offsets, p_cur,
                                       n_prompt, n_recent, scores, false, p);
@@ -294,31 +296,44 @@ tri_status tri_compress(const tri_kv* kv, const tri_centers* c, double rope_thet
                         tri_norm_mode norm_mode, const int32_t* offsets, int32_t n_offsets,
                         const int64_t* p_cur, int32_t n_prompt, int32_t n_recent, int32_t budget,
                         int32_t* keep_idx, void* ws, size_t ws_bytes, tri_stream_t stream) {
-  if (!kv) return TRI_ERR_INVALID_ARG;
+  TRI_CALL_RANGE();
+  tri_status st = check_kv(kv, true);
+  if (st != TRI_OK) return st;
   const size_t need = tri_compress_workspace_bytes(kv);
   if (need == 0 || ws_bytes < need || !ws || !aligned(ws, 16)) return TRI_ERR_INVALID_ARG;
   if (!kv->pos_out || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
-  tri_status st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
-  if (st != TRI_OK) return st;
   ScoreParams p;
   float* scores = static_cast<float*>(ws);
+  st = check_protect(n_prompt, n_recent, budget, kv->n_cap);
+  if (st != TRI_OK) return st;
   st = prepare_score(kv, c, rope_theta, style, norm_mode, offsets, n_offsets, p_cur, n_prompt, n_recent,
                      scores, true, p);
   if (st != TRI_OK) return st;
   const int n_slices = static_cast<int>(slices_of(kv));
+  const SelectParams ps = select_params(scores, kv, n_prompt, n_recent, budget, keep_idx);
+  const CompactParams pc = compact_params(kv, keep_idx, budget);
+  if (p.tiles_per_slice == 1) {
+    // A slice fits one score CTA: that CTA scores, selects and compacts it
+    // (one launch), so each slice's latency-bound selection overlaps other
+    // slices' score and row traffic.
+    const cudaError_t e = launch_compress_slices(p, ps, pc, kv->dtype, kv->head_dim, style, pos_mode(kv),
+                                                 n_slices, stream);
+    return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+  }
+  // Several score CTAs per slice: three kernels. Selecting in the last score
+  // CTA of each slice to finish measured slower: the score kernel is close to
+  // its issue limit, and a selecting CTA's slot stops streaming keys.
   cudaError_t e = launch_score(p, kv->dtype, kv->head_dim, style, pos_mode(kv), n_slices, stream);
   if (e != cudaSuccess) return TRI_ERR_CUDA;
-  // Selection and compaction as separate kernels: measured faster here than
-  // the fused kernel of tri_select_compact, whose CTAs cannot keep the
-  // copy rate while some of them are selecting.
-  e = launch_select(select_params(scores, kv, n_prompt, n_recent, budget, keep_idx), n_slices, stream);
+  e = launch_select(ps, n_slices, stream);
   if (e != cudaSuccess) return TRI_ERR_CUDA;
-  e = launch_compact(compact_params(kv, keep_idx, budget), n_slices, stream);
+  e = launch_compact(pc, n_slices, stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
 }
 
 tri_status tri_select_compact(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
                               int32_t budget, int32_t* keep_idx, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   tri_status st = check_kv(kv, true);
   if (st != TRI_OK) return st;
   if (!kv->pos_out || !scores || !aligned(scores, 4) || !keep_idx || !aligned(keep_idx, 4)) return TRI_ERR_INVALID_ARG;
@@ -333,6 +348,7 @@ tri_status tri_select_compact(const float* scores, const tri_kv* kv, int32_t n_p
 tri_status rand_evict_compact(const tri_kv* kv, uint64_t seed, uint32_t round, tri_draw_scope scope,
                               int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
                               tri_stream_t stream) {
+  TRI_CALL_RANGE();
   tri_status st = check_kv(kv, true);
   if (st != TRI_OK) return st;
   if (kv->n_layers > 65535 || kv->n_kv_heads > 65536) return TRI_ERR_INVALID_ARG;
@@ -353,6 +369,7 @@ tri_status rand_evict_compact(const tri_kv* kv, uint64_t seed, uint32_t round, t
 tri_status tri_select_topk(const float* scores, const tri_kv* kv, int32_t n_prompt,
                            int32_t n_recent, int32_t budget, int32_t* keep_idx,
                            tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (!kv) return TRI_ERR_INVALID_ARG;
   if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
   if (!kv->n_valid || !aligned(kv->n_valid, 4)) return TRI_ERR_INVALID_ARG;
@@ -367,12 +384,14 @@ tri_status tri_select_topk(const float* scores, const tri_kv* kv, int32_t n_prom
 
 tri_status rand_evict(const tri_kv* kv, uint64_t seed, uint32_t round, int32_t n_prompt,
                       int32_t n_recent, int32_t budget, int32_t* keep_idx, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   return rand_evict_scoped(kv, seed, round, TRI_DRAW_PER_HEAD, n_prompt, n_recent, budget, keep_idx, stream);
 }
 
 tri_status rand_evict_scoped(const tri_kv* kv, uint64_t seed, uint32_t round, tri_draw_scope scope,
                              int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
                              tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (!kv) return TRI_ERR_INVALID_ARG;
   if (scope != TRI_DRAW_PER_HEAD && scope != TRI_DRAW_PER_LAYER && scope != TRI_DRAW_PER_SEQUENCE)
     return TRI_ERR_INVALID_ARG;
@@ -392,6 +411,7 @@ tri_status rand_evict_scoped(const tri_kv* kv, uint64_t seed, uint32_t round, tr
 
 tri_status tri_compact_kv(const tri_kv* kv, const int32_t* keep_idx, int32_t budget,
                           tri_stream_t stream) {
+  TRI_CALL_RANGE();
   tri_status st = check_kv(kv, true);
   if (st != TRI_OK) return st;
   if (!kv->pos_out) return TRI_ERR_INVALID_ARG;
@@ -411,6 +431,7 @@ tri_status tri_score_heads(const tri_kv* kv, const tri_centers* centers, int32_t
                            tri_rope_style style, tri_norm_mode norm_mode, const int32_t* offsets,
                            int32_t n_offsets, const int64_t* p_cur, float* scores_g, float* stats,
                            void* ws, size_t ws_bytes, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (group < 1 || group > MAX_GROUP) return TRI_ERR_INVALID_ARG;
   if (!stats || !aligned(stats, 8)) return TRI_ERR_INVALID_ARG;
   ScoreParams p;
@@ -451,6 +472,7 @@ tri_status tri_score_heads(const tri_kv* kv, const tri_centers* centers, int32_t
 tri_status tri_select_topk_zmax(const float* scores_g, const float* stats, int32_t group, const tri_kv* kv,
                                 int32_t n_prompt, int32_t n_recent, int32_t budget, int32_t* keep_idx,
                                 float* final_scores, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (!kv) return TRI_ERR_INVALID_ARG;
   if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
   if (!kv->n_valid || !aligned(kv->n_valid, 4)) return TRI_ERR_INVALID_ARG;
@@ -511,6 +533,7 @@ size_t tri_select_union_workspace_bytes(const tri_kv* kv, int32_t n_prompt, int3
 tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_prompt, int32_t n_recent,
                             int32_t budget, int32_t k_head, int32_t* keep_idx, float* final_scores, void* ws,
                             size_t ws_bytes, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (!kv) return TRI_ERR_INVALID_ARG;
   if (kv->n_seq < 1 || kv->n_layers < 1 || kv->n_kv_heads < 1 || kv->n_cap < 1) return TRI_ERR_INVALID_ARG;
   if (kv->n_kv_heads > MAX_GROUP || kv->n_cap > UNION_MAX_CAP) return TRI_ERR_UNSUPPORTED;
@@ -567,6 +590,7 @@ tri_status tri_select_union(const float* scores, const tri_kv* kv, int32_t n_pro
 }
 
 tri_status tri_paged_blocks_used(const tri_kv* kv, int32_t* blocks_used, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   tri_status st = check_kv(kv, false);
   if (st != TRI_OK) return st;
   if (!kv->block_table || !blocks_used || !aligned(blocks_used, 4)) return TRI_ERR_INVALID_ARG;
@@ -575,6 +599,7 @@ tri_status tri_paged_blocks_used(const tri_kv* kv, int32_t* blocks_used, tri_str
 }
 
 tri_status tri_selftest_wait_timeout(int32_t* dev_status, uint64_t limit_ns, tri_stream_t stream) {
+  TRI_CALL_RANGE();
   if (!dev_status || !aligned(dev_status, 4) || limit_ns < 1000u || limit_ns > 1000000000u) return TRI_ERR_INVALID_ARG;
   const cudaError_t e = launch_wait_timeout_selftest(dev_status, limit_ns, stream);
   return e == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;

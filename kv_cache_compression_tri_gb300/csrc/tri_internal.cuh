@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/tri.h"
@@ -14,6 +15,18 @@ constexpr int MAX_BANDS = 64;  // head_dim <= 128
 
 // Count of kernels launched by the library (tri_launch_count).
 void note_launch();
+
+// An NVTX range named after the entry point, open for the call's host-side
+// part (argument checks and launches): a profiler that records NVTX shows
+// every library call on its timeline, named; without one the NVTX calls do
+// nothing (header-only NVTX v3, no library to link).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+#define TRI_CALL_RANGE() const ::tri::CallRange tri_call_range_(__func__)
 
 // First error wins: a device status word goes from 0 to `code` once.
 __device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
@@ -347,6 +360,11 @@ struct ScoreGeometry {
 };
 ScoreGeometry score_geometry(tri_dtype dt, int head_dim);
 cudaError_t launch_select(const SelectParams& p, int n_slices, cudaStream_t st);
+// Score (rows [P, n - W)), selection and compaction of every slice in one
+// launch, one CTA per slice; requires p.tiles_per_slice == 1.
+cudaError_t launch_compress_slices(const ScoreParams& p, const SelectParams& ps, const CompactParams& pc,
+                                   tri_dtype dt, int head_dim, tri_rope_style style, int pos_mode, int n_slices,
+                                   cudaStream_t st);
 // Per-query-head scores and per-CTA statistics partials, heads [head0, head0 +
 // n_heads) of every group; then the per-(slice, head) mean and standard
 // deviation; then (optional) the z-score maximum of every valid row.

@@ -205,3 +205,25 @@ def test_wait_timeout_selftest_rejects_bad_args(lib):
     assert f(0x10002, 1000000, None) == INVALID  # misaligned status word
     assert f(0x10000, 999, None) == INVALID  # limit below 1 us
     assert f(0x10000, 1000000001, None) == INVALID  # limit above 1 s
+
+
+def test_compress_rejects_bad_args(lib):
+    import kv_cache_compression_tri_gb300 as tri
+    kv = _kv()
+    c = tri._TriCenters(0x70000, 0x80000, 0x90000)
+    offs = (ctypes.c_int32 * 3)(1, 2, 4)
+    op = ctypes.cast(offs, ctypes.c_void_p)
+    cws = lib.tri_compress_workspace_bytes(ctypes.byref(kv))
+    assert cws == 2 * 128 * 4  # the scores
+    comp = lambda **o: lib.tri_compress(ctypes.byref(o.get("kv", kv)), ctypes.byref(c), 1e4, 0, 0, op, 3, 0xA0000,
+                                        o.get("P", 0), o.get("W", 0), o.get("budget", 64), o.get("keep", 0x50000),
+                                        o.get("ws", 0xC0000), o.get("ws_bytes", cws), None)
+    assert comp(ws_bytes=cws - 1) == INVALID
+    assert comp(ws=None) == INVALID
+    assert comp(ws=0xC0008) == INVALID  # the scores need 16-byte alignment
+    assert comp(keep=None) == INVALID
+    assert comp(P=40, W=40) == INVALID  # protected rows above the budget
+    assert comp(budget=129) == INVALID  # budget above n_cap
+    assert comp(kv=_kv(pos_out=None)) == INVALID
+    assert comp(kv=_kv(dtype=7)) == UNSUPPORTED
+    assert comp(kv=_kv(head_dim=96)) == UNSUPPORTED
