@@ -84,7 +84,8 @@ def test_gqa_stack_full_size():
         k = pk[s].to(torch.float64).numpy()
         ref = orc.score_heads(k, c[rows], m[rows], R[rows], w.offsets, int(p_cur[seq]), w.theta)
         Mg = np.stack([orc.score_bound(k, m[lh * G + g]) for g in range(G)])
-        assert np.all(np.abs(g_sc[s] - ref) <= SCORE_TOL * Mg), s
+        ratio = float((np.abs(g_sc[s] - ref) / Mg).max())
+        assert ratio <= SCORE_TOL, (s, ratio)
         mu, sd, fin = orc.zscore_max(ref)
         tol_st = SCORE_TOL * Mg.max(axis=1) + 1e-6 * (np.abs(mu) + sd)
         assert np.all(np.abs(g_st[s][:, 0] - mu) <= tol_st) and np.all(np.abs(g_st[s][:, 1] - sd) <= tol_st)
@@ -98,8 +99,16 @@ def test_gqa_stack_full_size():
         rows_np = pk[s].view(torch.int16).numpy().copy()
         orc.compact(rows_np, keep_all[s])
         assert np.array_equal(rows_np[:B], slice_rows(kv.k, s)[:B].cpu().view(torch.int16).numpy())
+        return ratio
 
-    pmap(check, sample)
+    # The tensor-core path rounds each key feature (Re z_f, -Im z_f, |k_f|) to
+    # fp16 once (2^-11 relative) and keeps the coefficients to about fp32
+    # (hi + lo fp16 pair): |error| <= 2^-11 * sqrt(2) * M_g(i) plus fp32
+    # rounding of the sums. The observed margin is reported and held to that
+    # bound, well inside the 1e-3 tolerance.
+    worst = max(pmap(check, sample))
+    print(f"GQA per-head score: worst |error| / M_g = {worst:.2e} over {len(sample)} slices x {G} heads")
+    assert worst <= 2.0 ** -11 * np.sqrt(2.0) + 1e-5, worst
 
 
 def test_gqa_eight_heads_explicit_positions_long_slices():
@@ -220,8 +229,23 @@ def test_union_stack_full_size():
     for g in synth.sample_slices(groups, 8):
         s64 = scores[g * H:(g + 1) * H].cpu().numpy().astype(np.float64)
         fin = final[g].cpu().numpy()
-        _, _, comb = orc.zscore_max(s64)
-        assert np.all(np.abs(fin - comb) <= 1e-5 * (1 + np.abs(comb) + 50)), g
+        mu, sd, comb = orc.zscore_max(s64)
+        # The kernel's statistics: each of 256 threads sums its m = n / 256
+        # scores in fp32 (recursive summation: error <= (m - 1) 2^-24 sum |x|),
+        # the threads' sums are added in fp64, and mu_h, then sd_h (centred
+        # squares about the fp32 mean, again summed per thread in fp32, a
+        # relative error <= (m + 2) 2^-24 in the variance, half that in sd_h),
+        # are rounded to fp32. Then max_h (x - mu_h) * (1 / sd_h) in fp32
+        # (subtraction, reciprocal, product: one rounding each). To first
+        # order z_h moves by at most
+        #   2^-24 [(m + 1) mean|x_h| / sd_h + (m / 2 + 5) |z_h|],
+        # and the maximum over heads by at most the largest per-head change.
+        # Heads with sd_h = 0 give 0 on both sides.
+        m_t = -(-n // 256)
+        live = sd > 0
+        lead = float(np.max(np.abs(s64[live, :n]).mean(axis=1) / sd[live])) if live.any() else 0.0
+        tol = 2.0 ** -24 * ((m_t + 1) * lead + (m_t / 2 + 5) * np.abs(comb))
+        assert np.all(np.abs(fin - comb) <= tol), (g, float(np.max(np.abs(fin - comb) - tol)))
         member = orc.union_members(s64, P, W, k_head)
         assert np.array_equal(keep_all[g * H], orc.union_rank(member, fin.astype(np.float64), P, W, B)), g
 
