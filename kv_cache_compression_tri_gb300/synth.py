@@ -126,6 +126,11 @@ WORKLOADS["qwen3_8b_stack_post_rope_1seq"] = scaled(
     description="one sequence of the post-RoPE stack")
 WORKLOADS["periodic_1seq"] = scaled(WORKLOADS["periodic_large_batch"], name="periodic_1seq", n_seq=1,
                                     description="one sequence of the large-batch periodic workload")
+# Profiling case for the periodic rounds' shape (2176 rows -> 2048, one
+# score CTA per slice): four sequences, 0.43 GB of K and V (more than L2).
+WORKLOADS["periodic_round_4seq"] = scaled(WORKLOADS["periodic_large_batch"], name="periodic_round_4seq", n_seq=4,
+                                          n_cap=2176, n_valid=2176, rounds=0,
+                                          description="four sequences of a periodic round: 2176 rows -> 2048")
 
 
 def _unit_rows(g: torch.Generator, shape, norm: float, device) -> torch.Tensor:
