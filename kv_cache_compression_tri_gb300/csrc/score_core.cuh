@@ -34,6 +34,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "score_common.cuh"
 #include "tri_internal.cuh"
 
@@ -191,27 +193,35 @@ __device__ __forceinline__ void score_cta(const ScoreParams& p, unsigned char* s
   float* out = p.scores + s * static_cast<int64_t>(p.n_cap);
   const int32_t* pos = EXPLICIT_POS ? p.pos + s * static_cast<int64_t>(p.n_cap) : nullptr;
 
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % STAGES;
-    // a warp whose wait timed out still reaches the barrier below
-    if (ring_wait(rc, t, lane)) {
-      const unsigned char* tile = ring + st * TILE_BYTES;
+  // One tile's keys of this lane. FULL: every row of the tile lies in the
+  // run (all tiles but possibly the last), so no key needs a range check.
+  // Only contiguous caches with slot or post-RoPE positions take a separate
+  // full-tile body: for paged caches and explicit positions the second copy
+  // of the larger body measured slower.
+  auto score_tile = [&](const int t, auto full_tag) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    {
+      const unsigned char* tile = ring + (t % STAGES) * TILE_BYTES;
       const int rbase = warp * RPW + kq;  // row within the tile of this lane's first key
       int pp[STEPS];
       if (EXPLICIT_POS) {
 #pragma unroll
         for (int j = 0; j < STEPS; ++j) {
           const int r = c0 + t * TILE_ROWS + rbase + j * KPW;
-          pp[j] = (r < c1) ? __ldg(pos + r) : 0;
+          pp[j] = (FULL || r < c1) ? __ldg(pos + r) : 0;
         }
       }
       float acc[STEPS];
 #pragma unroll
       for (int j = 0; j < STEPS; ++j) {
         const int rt = rbase + j * KPW;
-        const bool valid = c0 + t * TILE_ROWS + rt < c1;
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) raw = lds_chunk<T, D, STYLE>(tile + rt * ROW_BYTES, c);
+        uint4 raw;
+        if (FULL) {
+          raw = lds_chunk<T, D, STYLE>(tile + rt * ROW_BYTES, c);
+        } else {
+          raw = make_uint4(0u, 0u, 0u, 0u);
+          if (c0 + t * TILE_ROWS + rt < c1) raw = lds_chunk<T, D, STYLE>(tile + rt * ROW_BYTES, c);
+        }
         float re[BPT], im[BPT];
         decode_chunk<T, STYLE>(raw, re, im);
         float2 a2;  // starts with the first band pair's product (no zeroing)
@@ -255,8 +265,20 @@ __device__ __forceinline__ void score_cta(const ScoreParams& p, unsigned char* s
       int idx;
       const float v = reduce_scatter<TPK, STEPS>(acc, lane, idx);
       const int r = c0 + t * TILE_ROWS + rbase + idx * KPW;
-      if ((c % (TPK / STEPS)) == 0 && r < c1) {
+      if ((c % (TPK / STEPS)) == 0 && (FULL || r < c1)) {
         if (STREAM_OUT) __stcs(out + r, v); else out[r] = v;
+      }
+    }
+  };
+
+  for (int t = 0; t < ntiles; ++t) {
+    // a warp whose wait timed out still reaches the barrier below
+    if (ring_wait(rc, t, lane)) {
+      if constexpr (!PAGED && !EXPLICIT_POS) {
+        if (c0 + (t + 1) * TILE_ROWS <= c1) score_tile(t, std::true_type{});
+        else score_tile(t, std::false_type{});
+      } else {
+        score_tile(t, std::false_type{});
       }
     }
     // The kernel is near its issue limit and keeps its warps in step: the
