@@ -297,8 +297,8 @@ tri_status rand_evict_compact(const tri_kv* kv, uint64_t seed, uint32_t round, t
  * Exactly tri_score (rows [n_prompt, n_valid - n_recent)), tri_select_topk
  * and tri_compact_kv called in sequence with the same arguments, with the
  * scores kept in caller scratch. When a slice fits one CTA of the score
- * kernel (n_cap at most 2048 rows of 256 B, 4096 of 128 B, ...: 32 tiles of
- * 16 KB) one CTA scores, selects and compacts each slice in a single launch;
+ * kernel (n_cap at most 4096 rows of 256 B, 8192 of 128 B, ...: 32 tiles of
+ * 32 KB) one CTA scores, selects and compacts each slice in a single launch;
  * otherwise the three kernels run in turn.
  * keep_idx: device [n_slices][budget], written as by tri_select_topk.
  * ws: device scratch of at least tri_compress_workspace_bytes(kv) bytes,

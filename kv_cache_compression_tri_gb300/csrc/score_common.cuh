@@ -14,8 +14,8 @@ namespace {
 
 constexpr int SCORE_THREADS = 256;
 constexpr int SCORE_WARPS = SCORE_THREADS / 32;
-constexpr int STAGES = 4;
-constexpr int TILE_BYTES = 16384;
+constexpr int STAGES = 2;
+constexpr int TILE_BYTES = 32768;
 constexpr size_t RING_BYTES = static_cast<size_t>(STAGES) * TILE_BYTES;
 
 // Control block of a CTA's tile ring of NST stages read by NW warps, placed
@@ -107,7 +107,7 @@ struct Geo {
   static constexpr int TILE_ROWS = TILE_BYTES / ROW_BYTES;
   static constexpr int RPW = TILE_ROWS / SCORE_WARPS;  // rows per warp per tile
   static constexpr int STEPS = RPW / KPW;              // keys per lane per tile
-  static_assert(STEPS == 4 && TPK >= STEPS && TPK <= 32, "score geometry");
+  static_assert(STEPS >= 4 && TPK >= STEPS && TPK <= 32, "score geometry");
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }

@@ -11,11 +11,12 @@
 // (1/|D|) sum_delta [S_trig(k, age + delta) + S_norm(k)] exactly.
 //
 // Design (HBM-bound streaming):
-//   * one CTA streams a contiguous run of a slice's rows through a 4-stage
-//     ring of 16 KB shared-memory tiles, each filled by one bulk async copy
+//   * one CTA streams a contiguous run of a slice's rows through a 2-stage
+//     ring of 32 KB shared-memory tiles, each filled by one bulk async copy
 //     (TMA, non-tensor) that completes on an mbarrier; thread 0 refills a
-//     stage as soon as the CTA has consumed it, so 64 KB per CTA (192 KB per
-//     SM) are always in flight;
+//     stage as soon as the CTA has consumed it (64 KB per CTA, 192 KB per
+//     SM; 32 KB tiles amortise each tile's waits, barrier and reduction over
+//     twice the keys of 16 KB ones);
 //   * a key row is split across TPK lanes, each lane owning BPT consecutive
 //     bands (one 16-byte shared load per key); band constants live in
 //     registers as fp32 pairs so that two bands share one paired

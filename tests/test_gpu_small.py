@@ -482,9 +482,9 @@ def _compress_vs_separate(w, ragged=False, explicit_pos=False, seed=0, style=0):
     n0 = tri.launch_count()
     tri.compress(kv_b, c, w.theta, w.offsets, inp.p_cur, P, W, B, keep_b, workspace=ws, style=style)
     torch.cuda.synchronize()
-    # a slice that fits one score CTA: score, selection and compaction in one
-    # launch; else the three kernels
-    tile_rows = 16384 // (w.head_dim * w.elem_bytes)
+    # a slice that fits one score CTA (32 tiles of 32 KB): score, selection and
+    # compaction in one launch; else the three kernels
+    tile_rows = 32768 // (w.head_dim * w.elem_bytes)
     rows_per_cta = min(32 * tile_rows, -(-n_cap // tile_rows) * tile_rows)
     assert tri.launch_count() - n0 == (1 if n_cap <= rows_per_cta else 3)
     # tri_select_compact on the separate call's scores: the same again
