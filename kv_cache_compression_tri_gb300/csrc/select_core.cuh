@@ -296,6 +296,7 @@ struct ScoreKeys {
   static constexpr int U = 4;  // 16-byte loads in flight per thread
   static constexpr bool GROUPED = false;
   static constexpr bool INTERIOR = true;  // fetch_interior() for groups inside [P, end)
+  static constexpr bool PREFETCH = true;  // prefetch() the candidates' scores into L2
   const float* row;
   bool vec;  // 16-byte loads allowed
 
@@ -344,6 +345,19 @@ struct ScoreKeys {
     for (int e = 0; e < 4; ++e) k[e] = in_range(i0 + e, P, end) ? score_key(x[e], nan) : 0u;
     return make_uint4(k[0], k[1], k[2], k[3]);
   }
+  // One bulk prefetch into L2 of the candidates' scores (the whole 16-byte
+  // units inside [lo, end) of the row), so that the sample and the pass
+  // mostly hit L2 instead of waiting on DRAM one round trip at a time.
+  __device__ void prefetch(const Ctx& c) const {
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(row + c.lo) + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t b = reinterpret_cast<uintptr_t>(row + c.end) & ~static_cast<uintptr_t>(15);
+    if (b > a) {
+      uint64_t ga;
+      asm volatile("cvta.to.global.u64 %0, %1;" : "=l"(ga) : "l"(static_cast<uint64_t>(a)));
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ga), "r"(static_cast<uint32_t>(b - a))
+                   : "memory");
+    }
+  }
   __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
     const float* r = row;
     sampled_window<1>(sm, c, need, m, [r](int slot) {
@@ -358,6 +372,7 @@ struct DrawKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = false;
   static constexpr bool INTERIOR = false;
+  static constexpr bool PREFETCH = false;
   uint4 ctr;  // counter words 1..3 (head + 65536 layer, seq, round)
   uint2 key;
 
@@ -399,6 +414,7 @@ struct ZMaxKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = false;
   static constexpr bool INTERIOR = true;
+  static constexpr bool PREFETCH = false;
   const float* base;  // row 0 of the G score rows
   int64_t n_cap;
   float mu[G], inv[G];
@@ -516,6 +532,7 @@ struct UnionKeys {
   static constexpr int U = 1;
   static constexpr bool GROUPED = true;
   static constexpr bool INTERIOR = true;
+  static constexpr bool PREFETCH = false;
   ZMaxKeys<H> z;
   const uint32_t* member;  // the group's union bitmap, bit i = slot i
   bool many;
@@ -639,6 +656,9 @@ __device__ __forceinline__ void select_slice(const SelectParams& p, SSmem& sm, i
   if (need_total == 0) return;
   const int m = c.end - c.P;  // candidates
   const Src src = Src::make(p, c, seq, layer, head);
+  if constexpr (Src::PREFETCH) {
+    if (t == 0) src.prefetch(c);
+  }
   // the bitmaps cover every candidate: the pass fills them directly
   const bool direct = (c.end - c.lo) <= BM_SLOTS;
   bool nan = false;
