@@ -7,6 +7,10 @@
 namespace tri {
 namespace {
 
+// Four paged CTAs per SM: dynamic shared memory, the static part (one
+// 128-byte unit) and the 1 KB the SM reserves per CTA, within its 228 KB.
+static_assert(4 * (COMPACT_SMEM + CTAB * sizeof(int32_t) + 128 + 1024) <= 228 * 1024, "paged compaction occupancy");
+
 template <bool PAGED>
 __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ CompactParams p) {
   extern __shared__ __align__(128) unsigned char smem[];

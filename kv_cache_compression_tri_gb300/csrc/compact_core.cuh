@@ -41,7 +41,12 @@ constexpr int CSTAGES = 3;
 constexpr int CTILE = 8192;
 constexpr size_t CRING_BYTES = CSTAGES * CTILE;
 constexpr size_t COMPACT_SMEM = 2 * CRING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
-constexpr int CTAB = 2048;  // paged: table entries cached in shared memory (more are read from global)
+// Paged: table entries cached in shared memory, from the block of the first
+// row that moves (later ones are read from global). 2000 entries keep a paged
+// compaction CTA within a quarter of the SM's 228 KB (with the 1 KB each CTA
+// reserves), so four run per SM as in the contiguous case; 2048 would drop it
+// to three.
+constexpr int CTAB = 2000;
 constexpr int POS_PER_THREAD = 8;
 
 // A keep entry: through the read-only cache when the list is read-only for
@@ -56,11 +61,16 @@ __device__ __forceinline__ int keep_at(const int32_t* keep, int j) {
 // Row r of the slice is at pool + rows.row(sbase, trow, r).
 template <bool PAGED, bool RO>
 __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_t sbase, const int32_t* trow,
-                                          const int32_t* ctab, unsigned char* ring, uint64_t* full,
+                                          const int32_t* ctab, int cb0, unsigned char* ring, uint64_t* full,
                                           const int32_t* keep, int first, int n_keep, int rb, int lane,
                                           int32_t* dev_status) {
-  // paged row offsets: from the table cached in shared memory when it fit
-  auto paged_row = [&](int r) { return ctab ? rows.row_cached(sbase, ctab, 0, r) : rows.row(sbase, trow, r); };
+  // paged row offsets (rows >= first): entries of blocks cb0 .. cb0 + CTAB - 1
+  // from the copy in shared memory, later ones from the table
+  auto paged_row = [&](int r) {
+    const int i = (r >> rows.block_shift) - cb0;
+    const int64_t blk = (i < CTAB) ? ctab[i] : __ldg(trow + (r >> rows.block_shift));
+    return sbase + blk * rows.block_bytes + static_cast<int64_t>(r & (rows.block_size - 1)) * rows.row_bytes;
+  };
   const int TR = CTILE / rb;  // rows per tile
   const int u_first = first / TR;
   const int ntiles = (n_keep - 1) / TR - u_first + 1;
@@ -87,7 +97,7 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
 #pragma unroll
     for (int r = 0; r < RPL; ++r) {
       const int j = lo_j + lane + 32 * r;
-      const int src = (k < ntiles && j < hi_j) ? keep_at<RO>(keep, j) : 0;
+      const int src = (k < ntiles && j < hi_j) ? keep_at<RO>(keep, j) : first;  // first: any row that moves
       kv[r] = PAGED ? paged_row(src) : sbase + static_cast<int64_t>(src) * rb;
     }
   };
@@ -249,9 +259,11 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   const int64_t sbase = p.rows.slice_base(s);
   const int32_t* trow = p.rows.seq_table(s);
   const int r1 = max(sm.last_src + 1, n_keep);
-  int32_t* ctab = (PAGED && r1 > 0 && ((r1 - 1) >> p.rows.block_shift) < CTAB)
-                      ? reinterpret_cast<int32_t*>(smem + COMPACT_SMEM) : nullptr;
-  if (PAGED && !p.rows.blocks_ok(trow, 0, r1, &sm.bad_block, ctab)) {
+  // rows below `first` are neither read nor written, but every entry up to
+  // r1 is checked; the cache holds the entries from first's block on
+  const int cb0 = first >> p.rows.block_shift;
+  int32_t* ctab = PAGED ? reinterpret_cast<int32_t*>(smem + COMPACT_SMEM) : nullptr;
+  if (PAGED && !p.rows.blocks_ok(trow, 0, r1, &sm.bad_block, ctab, cb0, CTAB)) {
     if (t == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
     return;
   }
@@ -260,7 +272,7 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   if (wid < 2) {
     // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
     if (first < n_keep)
-      move_rows<PAGED, RO>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, smem + wid * CRING_BYTES,
+      move_rows<PAGED, RO>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, cb0, smem + wid * CRING_BYTES,
                 reinterpret_cast<uint64_t*>(smem + 2 * CRING_BYTES) + wid * CSTAGES, keep, first, n_keep,
                 p.row_bytes, lane, p.dev_status);
     return;

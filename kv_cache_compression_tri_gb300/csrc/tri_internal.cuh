@@ -232,28 +232,26 @@ struct RowMap {
     return table ? min(limit, block_size - (r & (block_size - 1))) : limit;
   }
   // every table entry for rows [r0, r1) lies in [0, num_blocks) (by the CTA;
-  // uniform result). When `cache` is given (room for the entries of blocks
-  // r0 / block_size .. (r1 - 1) / block_size), the entries are kept there.
+  // uniform result). When `cache` is given, the entries of blocks cache_b0 ..
+  // cache_b0 + cache_n - 1 among them are kept there (cache_b0 < 0: from the
+  // block of row r0; by default every entry checked).
   __device__ __forceinline__ bool blocks_ok(const int32_t* trow, int r0, int r1, int* sflag,
-                                            int32_t* cache = nullptr) const {
+                                            int32_t* cache = nullptr, int cache_b0 = -1,
+                                            int cache_n = 0x7fffffff) const {
     if (!table || r0 >= r1) return true;
     if (threadIdx.x == 0) *sflag = 0;
     __syncthreads();
     const int b0 = r0 >> block_shift;
+    const int cb0 = cache_b0 < 0 ? b0 : cache_b0;
     for (int b = b0 + static_cast<int>(threadIdx.x); b <= ((r1 - 1) >> block_shift); b += static_cast<int>(blockDim.x)) {
       const int v = __ldg(trow + b);
       if (v < 0 || v >= num_blocks) *sflag = 1;
-      if (cache) cache[b - b0] = v;
+      if (cache && b >= cb0 && b - cb0 < cache_n) cache[b - cb0] = v;
     }
     __syncthreads();
     const bool ok = *sflag == 0;
     __syncthreads();
     return ok;
-  }
-  // byte offset of row r from a cached table (entry of block b at cache[b - b0])
-  __device__ __forceinline__ int64_t row_cached(int64_t base, const int32_t* cache, int b0, int r) const {
-    return base + static_cast<int64_t>(cache[(r >> block_shift) - b0]) * block_bytes +
-           static_cast<int64_t>(r & (block_size - 1)) * row_bytes;
   }
 };
 
