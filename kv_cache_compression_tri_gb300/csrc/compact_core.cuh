@@ -97,7 +97,8 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
 #pragma unroll
     for (int r = 0; r < RPL; ++r) {
       const int j = lo_j + lane + 32 * r;
-      const int src = (k < ntiles && j < hi_j) ? keep_at<RO>(keep, j) : first;  // first: any row that moves
+      // (paged: a row that moves, so that its table entry is in the cache's range)
+      const int src = (k < ntiles && j < hi_j) ? keep_at<RO>(keep, j) : (PAGED ? first : 0);
       kv[r] = PAGED ? paged_row(src) : sbase + static_cast<int64_t>(src) * rb;
     }
   };
