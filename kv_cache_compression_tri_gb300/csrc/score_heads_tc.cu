@@ -85,6 +85,7 @@ constexpr int TC_HPW = TC_HEADS / TC_HSPLIT;           // heads one read-out war
 constexpr int TC_NBUF = 3;       // operand buffers and accumulators, used by block index mod 3
 constexpr int TC_TMEM_COLS = 64;  // three accumulators of 16 columns (allocations are powers of two)
 constexpr int TC_ROWS_PER_CTA = 16384;
+constexpr int TC_PREFETCH = 6;  // tiles the copy warp prefetches into L2 ahead of the ring's newest
 constexpr uint32_t TC_IDESC = f16_idesc(TC_M, TC_N);
 
 template <int D>
@@ -146,6 +147,14 @@ struct TcLayout {
   // coefficient scratch [TC_HEADS][F][3] floats, in A before the first block
   static_assert(TC_HEADS * G::F * 3 * sizeof(float) <= static_cast<size_t>(G::A_BYTES), "coefficients fit");
 };
+
+// Bulk prefetch of [p, p + bytes) into L2 (both 16-byte aligned): no shared
+// memory, no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  uint64_t ga;
+  asm volatile("cvta.to.global.u64 %0, %1;" : "=l"(ga) : "l"(reinterpret_cast<uint64_t>(p)));
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ga), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -266,8 +275,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   }
   // ---- the copy warp: one thread streams the tiles through the ring -------
+  // The ring holds one tile per group, which alone would leave the SM with
+  // two tiles' bytes in flight from DRAM; tiles up to TC_PREFETCH beyond the
+  // newest one in the ring are prefetched into L2, so the ring's own copies
+  // mostly wait on L2 rather than DRAM.
   if (warp == TC_COPY_WARP) {
     if (lane == 0) {
+      auto prefetch_tile = [&](int u) {
+        const int r0 = c0 + u * TILE_ROWS;
+        const int rows = min(TILE_ROWS, c1 - r0);
+        for (int done = 0; done < rows;) {
+          const int run = p.rows.run(r0 + done, rows - done);
+          prefetch_l2(kbase + p.rows.row(sbase, trow, r0 + done), static_cast<uint32_t>(run * ROW_BYTES));
+          done += run;
+        }
+      };
+      for (int u = NST; u < min(ntiles, NST + TC_PREFETCH); ++u) prefetch_tile(u);
       for (int u = 0; u < ntiles; ++u) {
         const int st = u % NST;
         if (u >= NST && !mbar_wait_sleep(&ctrl.empty[st], static_cast<uint32_t>((u / NST - 1) & 1))) {
@@ -287,6 +310,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           done += run;
         }
         ctrl.issued = u + 1;
+        if (u >= NST && u + TC_PREFETCH < ntiles) prefetch_tile(u + TC_PREFETCH);
       }
     }
   } else {
