@@ -2,8 +2,8 @@
 // by one CTA (compact.cu launches it alone, select_compact.cu after the
 // slice's selection in the same CTA).
 //
-// Random Attention, Appendix F: keep-sets are sorted chronologically and the
-// KV tensors are compacted with a gather. Semantics: for j = 0, 1, ...,
+// Random Attention, Appendix F: each head's kept slots, put back in time
+// order, are gathered to the front of its K and V. Semantics: for j = 0, 1, ...,
 // n_keep-1 in order, row j <- row keep[j]. keep is ascending with
 // keep[j] >= j, so the source of destination j is never a row written by an
 // earlier destination, though it may be a row that a later destination

@@ -367,8 +367,8 @@ int orc_rand_select(uint64_t seed, uint32_t round, int64_t seq, int64_t layer, i
 // ---------------------------------------------------------------------------
 // GQA aggregation, [TA] "Handling Grouped-Query Attention (GQA)": each of the
 // G query heads that share a KV head scores every cached key with its own
-// centre statistics; per head g the mean mu_g and the standard deviation
-// sigma_g of its scores over all n cached keys turn them into z-scores, and
+// centre statistics; head g's scores are standardised with their own mean
+// mu_g and standard deviation sigma_g (taken over the n keys in the cache), and
 // the final score of a key is the largest z-score over the G heads.
 // Readings: sigma_g is the population standard deviation (sum over n, divided
 // by n); the choice scales every head of a slice alike, so no selection can
