@@ -14,7 +14,7 @@ static_assert(4 * (COMPACT_SMEM + CTAB * sizeof(int32_t) + 128 + 1024) <= 228 * 
 template <bool PAGED>
 __global__ void __launch_bounds__(CT) compact_kernel(const __grid_constant__ CompactParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  compact_slice<PAGED, CT, true>(p, smem, blockIdx.x);
+  compact_slice<PAGED, CT, true>(p, CompactSmem<CSTAGES>::packed(smem), blockIdx.x);
 }
 
 // One thread per sequence: blocks still holding live rows after compaction.

@@ -41,6 +41,22 @@ constexpr int CSTAGES = 3;
 constexpr int CTILE = 8192;
 constexpr size_t CRING_BYTES = CSTAGES * CTILE;
 constexpr size_t COMPACT_SMEM = 2 * CRING_BYTES + 2 * CSTAGES * sizeof(uint64_t);
+
+// Where a compaction CTA keeps its shared state: the K and V rings (NST
+// tiles each, V's right after K's), 2 NST mbarriers, and for a paged cache
+// the copy of CTAB table entries.
+template <int NST>
+struct CompactSmem {
+  unsigned char* rings;
+  uint64_t* bars;
+  int32_t* ctab;
+  static constexpr size_t RING = static_cast<size_t>(NST) * CTILE;  // one tensor's
+  static constexpr size_t BARS = 2 * NST * sizeof(uint64_t);
+  // the standalone kernels' layout: rings, then mbarriers, then the table
+  __device__ static CompactSmem packed(unsigned char* smem) {
+    return {smem, reinterpret_cast<uint64_t*>(smem + 2 * RING), reinterpret_cast<int32_t*>(smem + 2 * RING + BARS)};
+  }
+};
 // Paged: table entries cached in shared memory, from the block of the first
 // row that moves (later ones are read from global). 2000 entries keep a paged
 // compaction CTA within a quarter of the SM's 228 KB (with the 1 KB each CTA
@@ -57,9 +73,9 @@ __device__ __forceinline__ int keep_at(const int32_t* keep, int j) {
 }
 
 // Rows [first, n_keep) of one tensor of one slice, moved by one warp
-// through a ring of CSTAGES tiles of CTILE bytes (see the file comment).
+// through a ring of NST tiles of CTILE bytes (see the file comment).
 // Row r of the slice is at pool + rows.row(sbase, trow, r).
-template <bool PAGED, bool RO>
+template <bool PAGED, bool RO, int NST>
 __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_t sbase, const int32_t* trow,
                                           const int32_t* ctab, int cb0, unsigned char* ring, uint64_t* full,
                                           const int32_t* keep, int first, int n_keep, int rb, int lane,
@@ -76,7 +92,7 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
   const int ntiles = (n_keep - 1) / TR - u_first + 1;
   if (lane == 0) {
 #pragma unroll
-    for (int st = 0; st < CSTAGES; ++st) mbar_init(&full[st], 1);
+    for (int st = 0; st < NST; ++st) mbar_init(&full[st], 1);
     mbar_init_fence();
   }
   __syncwarp();
@@ -105,7 +121,7 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
   auto gather = [&](int k, const int64_t (&kv)[RPL]) {
     int lo_j, hi_j, t0;
     rows_of(k, lo_j, hi_j, t0);
-    const int st = k % CSTAGES;
+    const int st = k % NST;
     if (lane == 0) mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((hi_j - lo_j) * rb));
     __syncwarp();
     // Rows lo_j + 32 r + (0..31) sit in lanes 0..31. A row whose source
@@ -127,17 +143,17 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
     }
   };
 
-  for (int k = 0; k < min(CSTAGES - 1, ntiles); ++k) {
+  for (int k = 0; k < min(NST - 1, ntiles); ++k) {
     int64_t kv[RPL];
     load_keep(k, kv);
     gather(k, kv);
   }
-  load_keep(CSTAGES - 1, knext);
+  load_keep(NST - 1, knext);
   int k = 0;
   bool ok = true;
   for (; k < ntiles; ++k) {
-    const int st = k % CSTAGES;
-    ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / CSTAGES) & 1));
+    const int st = k % NST;
+    ok = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / NST) & 1));
     ok = __all_sync(FULL_MASK, ok);
     if (!ok) break;
     if (lane == 0) {
@@ -157,7 +173,7 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
       }
       bulk_commit();
     }
-    const int kn = k + CSTAGES - 1;  // refills the stage of tile k - 1
+    const int kn = k + NST - 1;  // refills the stage of tile k - 1
     if (kn < ntiles) {
       int64_t kv[RPL];
 #pragma unroll
@@ -172,8 +188,8 @@ __device__ __forceinline__ void move_rows(char* pool, const RowMap& rows, int64_
     // A gather never landed: report it and let the copies in flight finish
     // before the CTA's shared memory is released.
     set_status(dev_status, TRI_DEV_TIMEOUT);
-    for (int u = k; u < min(ntiles, k + CSTAGES - 1); ++u)
-      (void)mbar_wait_bounded(&full[u % CSTAGES], static_cast<uint32_t>((u / CSTAGES) & 1));
+    for (int u = k; u < min(ntiles, k + NST - 1); ++u)
+      (void)mbar_wait_bounded(&full[u % NST], static_cast<uint32_t>((u / NST) & 1));
   }
   if (lane == 0) bulk_wait_all();
 }
@@ -187,11 +203,11 @@ struct CSmem {
 };
 
 // Slice s, by a CTA of NTH threads (NTH >= 128): warps 0 and 1 move the K
-// and V rows, the other warps the positions. smem: COMPACT_SMEM bytes (plus
-// CTAB entries for a paged cache). RO: the keep list is read-only for the
-// whole kernel (else it was written earlier in the same kernel).
-template <bool PAGED, int NTH, bool RO>
-__device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned char* smem, int64_t s) {
+// and V rows through rings of NST tiles, the other warps the positions.
+// RO: the keep list is read-only for the whole kernel (else it was written
+// earlier in the same kernel).
+template <bool PAGED, int NTH, bool RO, int NST = CSTAGES>
+__device__ __forceinline__ void compact_slice(const CompactParams& p, const CompactSmem<NST>& cs, int64_t s) {
   static_assert(NTH >= 128 && NTH % 32 == 0, "compaction CTA");
   __shared__ CSmem sm;
   const int t = threadIdx.x, lane = t & 31;
@@ -263,7 +279,7 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   // rows below `first` are neither read nor written, but every entry up to
   // r1 is checked; the cache holds the entries from first's block on
   const int cb0 = first >> p.rows.block_shift;
-  int32_t* ctab = PAGED ? reinterpret_cast<int32_t*>(smem + COMPACT_SMEM) : nullptr;
+  int32_t* ctab = PAGED ? cs.ctab : nullptr;
   if (PAGED && !p.rows.blocks_ok(trow, 0, r1, &sm.bad_block, ctab, cb0, CTAB)) {
     if (t == 0) set_status(p.dev_status, TRI_DEV_BAD_BLOCK);
     return;
@@ -273,9 +289,8 @@ __device__ __forceinline__ void compact_slice(const CompactParams& p, unsigned c
   if (wid < 2) {
     // warp 0 moves the K rows, warp 1 the V rows, each through its own ring
     if (first < n_keep)
-      move_rows<PAGED, RO>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, cb0, smem + wid * CRING_BYTES,
-                reinterpret_cast<uint64_t*>(smem + 2 * CRING_BYTES) + wid * CSTAGES, keep, first, n_keep,
-                p.row_bytes, lane, p.dev_status);
+      move_rows<PAGED, RO, NST>(wid == 0 ? p.k : p.v, p.rows, sbase, trow, ctab, cb0, cs.rings + wid * cs.RING,
+                                cs.bars + wid * NST, keep, first, n_keep, p.row_bytes, lane, p.dev_status);
     return;
   }
   // the other warps move the positions meanwhile

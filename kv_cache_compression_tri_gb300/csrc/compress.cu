@@ -19,12 +19,23 @@
 namespace tri {
 namespace {
 
-// The selection's and the compaction's shared memory overlay the score
-// ring's tiles only (not the ring's mbarriers after them), so no barrier
-// object is repurposed; the three phases use one CTA shape.
+// The selection's state and the compaction's rings overlay the score ring's
+// tiles only; the compaction's mbarriers and a paged cache's table copy come
+// after the score ring's control block, so no barrier object is repurposed.
+// The three phases use one CTA shape. Three CTAs share an SM (registers), so
+// the compaction takes four ring stages per tensor here (the standalone
+// kernel, at four CTAs per SM, has three): more bytes in flight while the
+// SM's other CTAs score or select.
+constexpr int FUSED_CSTAGES = 4;
+using FusedCompactSmem = CompactSmem<FUSED_CSTAGES>;
 static_assert(sizeof(SSmem) <= RING_BYTES, "selection state must fit in the score ring's tiles");
-static_assert(COMPACT_SMEM + CTAB * sizeof(int32_t) <= RING_BYTES, "compaction state must fit in the score ring's tiles");
+static_assert(2 * FusedCompactSmem::RING <= RING_BYTES, "compaction rings must fit in the score ring's tiles");
+static_assert(SCORE_SMEM % 16 == 0, "compaction mbarriers after the score ring's control block");
 static_assert(NT == SCORE_THREADS, "one CTA shape for the score and the selection");
+
+constexpr size_t fused_smem(bool paged) {
+  return SCORE_SMEM + FusedCompactSmem::BARS + (paged ? CTAB * sizeof(int32_t) : 0);
+}
 
 template <typename T, int D, int STYLE, int PM, bool PAGED>
 __global__ void __launch_bounds__(SCORE_THREADS, 3)
@@ -38,18 +49,20 @@ __global__ void __launch_bounds__(SCORE_THREADS, 3)
   const int n = ps.n_valid[s];
   __syncthreads();  // the keep list is written; the selection's shared memory is free
   if (n > ps.n_cap || n < 0) return;  // the selection reported it and wrote no list
-  compact_slice<PAGED, SCORE_THREADS, false>(pc, smem, s);
+  const FusedCompactSmem cs{smem, reinterpret_cast<uint64_t*>(smem + SCORE_SMEM),
+                            reinterpret_cast<int32_t*>(smem + SCORE_SMEM + FusedCompactSmem::BARS)};
+  compact_slice<PAGED, SCORE_THREADS, false, FUSED_CSTAGES>(pc, cs, s);
 }
 
 template <typename T, int D, int STYLE, int PM>
 cudaError_t launch_one(const ScoreParams& p, const SelectParams& ps, const CompactParams& pc, int n_slices,
                        cudaStream_t st) {
-  auto kern = p.rows.table ? compress_slice_kernel<T, D, STYLE, PM, true>
-                           : compress_slice_kernel<T, D, STYLE, PM, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SCORE_SMEM));
+  const bool paged = p.rows.table != nullptr;
+  auto kern = paged ? compress_slice_kernel<T, D, STYLE, PM, true> : compress_slice_kernel<T, D, STYLE, PM, false>;
+  const size_t smem = fused_smem(paged);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(n_slices), SCORE_THREADS, SCORE_SMEM, st>>>(p, ps, pc);
+  kern<<<static_cast<unsigned>(n_slices), SCORE_THREADS, smem, st>>>(p, ps, pc);
   note_launch();
   return cudaGetLastError();
 }

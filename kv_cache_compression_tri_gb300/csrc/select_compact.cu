@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(NT, 3)
   const int n = ps.n_valid[s];
   __syncthreads();  // the keep list is written; the selection's shared memory is free
   if (n > ps.n_cap || n < 0) return;  // the selection reported it and wrote no list
-  compact_slice<PAGED, NT, false>(pc, smem, s);
+  compact_slice<PAGED, NT, false>(pc, CompactSmem<CSTAGES>::packed(smem), s);
 }
 
 template <class Src>
