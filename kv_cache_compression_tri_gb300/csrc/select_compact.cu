@@ -2,7 +2,9 @@
 //
 // The compaction (compact_core.cuh) streams rows at the copy rate with little
 // instruction issue; the selection (select_core.cuh) is latency-bound with
-// little traffic. Running both per slice in one CTA, three CTAs per SM, lets
+// little traffic. Running both per slice in one CTA, four CTAs per SM (64
+// registers; the compaction's three-stage rings and the selection's state
+// share about 49 KB), lets
 // one slice's selection overlap other slices' row traffic instead of taking
 // its own pass over the GPU. Semantics are exactly the two calls in sequence
 // (tri_select_topk or rand_evict, then tri_compact_kv): the keep list is
