@@ -171,8 +171,8 @@ tri_status tri_calibrate_centers(const void* q, tri_dtype dtype, int32_t n_layer
 namespace tri {
 namespace {
 
-// Rows per CTA of the score kernels: ~512 KB of keys (32 tiles), fewer for
-// small caches; and the CTAs per slice.
+// Rows per CTA of the score kernels: 32 tiles (1 MB of keys at 32 KB tiles),
+// fewer for small caches; and the CTAs per slice.
 void score_tiling(const tri_kv* kv, int32_t& rows_per_cta, int32_t& tiles_per_slice) {
   const ScoreGeometry g = score_geometry(kv->dtype, kv->head_dim);
   int rpc = 32 * g.tile_rows;
