@@ -193,6 +193,56 @@ def test_paged_gqa_compress_and_post_rope():
     assert torch.equal(scs[0], scs[1])
 
 
+def test_paged_compaction_past_the_shared_table_copy():
+    """A compaction CTA keeps the table entries of 2000 blocks (from the block
+    of the first row that moves) in shared memory and reads later ones from
+    the table: 32768-row slices in 16-row blocks with nothing protected use
+    both, through the standalone compaction and the fused random
+    selection + compaction."""
+    w = synth.scaled(LAYER, n_seq=1, n_layers=1, n_kv_heads=2, n_cap=32768, n_valid=32768, budget=4096,
+                     n_prompt=0, n_recent=64, n_cal=256)
+    inp = synth.make_inputs(w, "cuda")
+    S, n_cap, L, H, B, W, bs = w.n_slices, w.n_cap, w.n_layers, w.n_kv_heads, w.budget, w.n_recent, 16
+    assert n_cap // bs > 2000
+    c = tri.calibrate_centers(inp.q, w.group)
+    sc = torch.empty(S, n_cap, device="cuda")
+    tri.score(make_cache(inp), c, w.theta, w.offsets, inp.p_cur, sc, n_prompt=0, n_recent=W)
+    keep = torch.empty(S, B, dtype=torch.int32, device="cuda")
+    tri.select_topk(sc, make_cache(inp), 0, W, B, keep)
+    torch.cuda.synchronize()
+    before_k = [slice_rows(inp.k, s).clone() for s in range(S)]
+    keep_h = keep.cpu().numpy()
+    assert keep_h[:, 0].max() < 2000 * bs and keep_h[:, -1].min() >= 2000 * bs  # both halves of the table
+    for fused in (False, True):
+        kp, vp, table, _, _ = _paged_copy(inp, bs, seed=11 + fused)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kv_p = tri.PagedKVCache(kp, vp, table, inp.n_valid.clone(), None,
+                                torch.empty(S, n_cap, dtype=torch.int32, device="cuda"), st)
+        kv_c = tri.KVCache(inp.k.clone(), inp.v.clone(), inp.n_valid.clone(), None,
+                           torch.empty(S, n_cap, dtype=torch.int32, device="cuda"),
+                           torch.zeros(1, dtype=torch.int32, device="cuda"))
+        if fused:
+            kps, kcs = torch.empty_like(keep), torch.empty_like(keep)
+            tri.rand_evict_compact(kv_p, 5, 1, 0, W, B, kps)
+            tri.rand_evict_compact(kv_c, 5, 1, 0, W, B, kcs)
+        else:
+            kps = kcs = keep
+            tri.compact_kv(kv_p, keep, B)
+            tri.compact_kv(kv_c, keep, B)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0 and int(kv_c.dev_status.item()) == 0
+        assert torch.equal(kps, kcs) and torch.equal(kv_p.n_valid, kv_c.n_valid)
+        tab = table.cpu().numpy()
+        for s in range(S):
+            assert torch.equal(_logical(kp, tab, s, B, L, H, bs), slice_rows(kv_c.k, s)[:B]), (fused, s)
+            assert torch.equal(_logical(vp, tab, s, B, L, H, bs), slice_rows(kv_c.v, s)[:B]), (fused, s)
+            assert torch.equal(kv_p.pos_out[s, :B], kv_c.pos_out[s, :B])
+        # the oracle's in-place byte loop on the logical rows gives the same
+        rows = before_k[0].cpu().view(torch.int16).numpy().copy()
+        orc.compact(rows, kps[0].cpu().numpy())
+        assert np.array_equal(rows[:B], _logical(kp, tab, 0, B, L, H, bs).cpu().view(torch.int16).numpy())
+
+
 def test_paged_bad_block_entry_sets_status():
     # the bad entry names a block that is allocated (a spare past num_blocks),
     # so nothing can leave the pool even if the check were missing
