@@ -217,16 +217,23 @@ __device__ __forceinline__ void block_minmax(SSmem& sm, uint32_t& kmin, uint32_t
   __syncthreads();  // wmin / wmax may be rewritten by the next call
 }
 
+// The keys of RUN consecutive slots.
+template <int RUN>
+struct RunKeys {
+  uint32_t k[RUN];
+};
+
 // Window from a systematic sample of NSAMPLE candidates spread evenly over
 // [P, n - W), taken as NSAMPLE / RUN runs of RUN consecutive slots (each run
 // RUN-aligned). Sources that read one score row use RUN = 1; sources that
 // read several rows per slot use RUN = 8, one 32-byte sector per row, so the
 // sample touches an eighth of the sectors (their CTAs' rows do not stay in L2
-// until the pass re-reads them). key_of(slot) gives a slot's key. The sample
-// keys of ranks r* -+ SAMPLE_SD sd bound [t_lo, t_hi] (r* = need NSAMPLE / m,
-// sd its binomial standard deviation). Requires m > LCAP (>= 2 NSAMPLE slots).
-template <int RUN, class KeyOf>
-__device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const KeyOf& key_of, uint32_t& t_lo,
+// until the pass re-reads them). run_of(s0) gives the keys of slots s0 ..
+// s0 + RUN - 1. The sample keys of ranks r* -+ SAMPLE_SD sd bound [t_lo,
+// t_hi] (r* = need NSAMPLE / m, sd its binomial standard deviation). Requires
+// m > LCAP (>= 2 NSAMPLE slots).
+template <int RUN, class RunOf>
+__device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const RunOf& run_of, uint32_t& t_lo,
                                uint32_t& t_hi) {
   static_assert(SPT % RUN == 0, "runs per thread");
   constexpr int NRUN = NSAMPLE / RUN;
@@ -239,9 +246,10 @@ __device__ void sampled_window(SSmem& sm, const Ctx& c, int need, int m, const K
   for (int q = 0; q < SPT / RUN; ++q) {
     const int j = t + NT * q;  // run index
     const int run = first + static_cast<int>((static_cast<int64_t>(last - first) * j) / (NRUN - 1));
+    const RunKeys<RUN> rk = run_of(run * RUN);
 #pragma unroll
     for (int r = 0; r < RUN; ++r) {
-      sk[q * RUN + r] = key_of(run * RUN + r);
+      sk[q * RUN + r] = rk.k[r];
       kmin = min(kmin, sk[q * RUN + r]);
       kmax = max(kmax, sk[q * RUN + r]);
     }
@@ -362,7 +370,7 @@ struct ScoreKeys {
     const float* r = row;
     sampled_window<1>(sm, c, need, m, [r](int slot) {
       bool ignored = false;  // NaN is flagged by the full pass
-      return score_key(__ldcg(r + slot), ignored);
+      return RunKeys<1>{{score_key(__ldcg(r + slot), ignored)}};
     }, t_lo, t_hi);
   }
 };
@@ -510,11 +518,37 @@ struct ZMaxKeys {
     for (int e = 0; e < 4; ++e) k[e] = in_range(i0 + e, P, end) ? score_key(best[e], nan) : 0u;
     return make_uint4(k[0], k[1], k[2], k[3]);
   }
+  // max_g z_g of the 8 slots s0 .. s0+7 (s0 a multiple of 8, s0 + 7 < n_cap):
+  // two 16-byte loads per head row when the rows are 16-byte aligned, so the
+  // sample's loads do not crowd the load/store queue
+  __device__ __forceinline__ void best8(int s0, float (&best)[8]) const {
+    if (vec) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float4* q = reinterpret_cast<const float4*>(base + g * n_cap + s0);
+        const float4 a = __ldcg(q), b = __ldcg(q + 1);
+        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float z = head_z(x[e], mu[g], inv[g]);
+          best[e] = (g == 0) ? z : fmaxf(best[e], z);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) best[e] = final_score(s0 + e);
+    }
+  }
   __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
     const ZMaxKeys& self = *this;
-    sampled_window<8>(sm, c, need, m, [&self](int slot) {
+    sampled_window<8>(sm, c, need, m, [&self](int s0) {
+      float best[8];
+      self.best8(s0, best);
+      RunKeys<8> o;
       bool ignored = false;
-      return score_key(self.final_score(slot), ignored);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o.k[e] = score_key(best[e], ignored);
+      return o;
     }, t_lo, t_hi);
   }
 };
@@ -571,10 +605,15 @@ struct UnionKeys {
   }
   __device__ void window(SSmem& sm, const Ctx& c, int need, int m, uint32_t& t_lo, uint32_t& t_hi) const {
     const UnionKeys& self = *this;
-    sampled_window<8>(sm, c, need, m, [&self](int slot) {
+    sampled_window<8>(sm, c, need, m, [&self](int s0) {
+      float best[8];
+      self.z.best8(s0, best);
+      const uint32_t word = __ldg(self.member + (s0 >> 5)) >> (s0 & 31);  // s0 % 8 == 0: one word
+      RunKeys<8> o;
       bool ignored = false;
-      const bool in_union = (__ldg(self.member + (slot >> 5)) >> (slot & 31)) & 1u;
-      return self.key(in_union, self.z.final_score(slot), ignored);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o.k[e] = self.key((word >> e) & 1u, best[e], ignored);
+      return o;
     }, t_lo, t_hi);
   }
 };
