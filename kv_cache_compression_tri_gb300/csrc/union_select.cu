@@ -91,7 +91,10 @@ __global__ void __launch_bounds__(UT) union_prep_kernel(const __grid_constant__ 
 
 // One CTA per slice: mean and population standard deviation of its scores
 // over rows [0, n_valid) -- two passes (the mean, then the centred squares),
-// fp64 block sums in a fixed order.
+// fp64 block sums in a fixed order. A thread reads 16 bytes at a time when
+// the row is 16-byte aligned and keeps four fp32 partial sums (one per lane
+// of the load, each over at most n / 1024 + 1 scores), so its share of at
+// most n / 256 scores is summed in shorter chains than one running sum.
 __global__ void __launch_bounds__(UT) slice_stats_kernel(const float* __restrict__ scores,
                                                          const int32_t* __restrict__ n_valid, float* stats,
                                                          int n_cap) {
@@ -100,15 +103,36 @@ __global__ void __launch_bounds__(UT) slice_stats_kernel(const float* __restrict
   const int64_t s = blockIdx.x;
   const int n = min(max(n_valid[s], 0), n_cap);
   const float* row = scores + s * static_cast<int64_t>(n_cap);
-  float a = 0.f;
-  for (int i = t; i < n; i += UT) a += __ldcg(row + i);
-  const double mean = (n > 0) ? block_sum(a, sred) / n : 0.0;
-  const float mf = static_cast<float>(mean);
-  float b = 0.f;
-  for (int i = t; i < n; i += UT) {
-    const float d = __ldcg(row + i) - mf;
-    b = fmaf(d, d, b);
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+  const int n4 = vec ? (n >> 2) : 0;  // whole 16-byte units; the rest one by one
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+  for (int i = t; i < n4; i += UT) {
+    const float4 x = __ldcg(row4 + i);
+    a0 += x.x;
+    a1 += x.y;
+    a2 += x.z;
+    a3 += x.w;
   }
+  for (int i = 4 * n4 + t; i < n; i += UT) a0 += __ldcg(row + i);
+  const double mean = (n > 0) ? block_sum((a0 + a1) + (a2 + a3), sred) / n : 0.0;
+  const float mf = static_cast<float>(mean);
+  float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll 4
+  for (int i = t; i < n4; i += UT) {
+    const float4 x = __ldcg(row4 + i);
+    const float d0 = x.x - mf, d1 = x.y - mf, d2 = x.z - mf, d3 = x.w - mf;
+    b0 = fmaf(d0, d0, b0);
+    b1 = fmaf(d1, d1, b1);
+    b2 = fmaf(d2, d2, b2);
+    b3 = fmaf(d3, d3, b3);
+  }
+  for (int i = 4 * n4 + t; i < n; i += UT) {
+    const float d = __ldcg(row + i) - mf;
+    b0 = fmaf(d, d, b0);
+  }
+  const float b = (b0 + b1) + (b2 + b3);
   // the centred sum uses the fp32 mean; correct it to the fp64 one
   const double dm = mean - static_cast<double>(mf);
   const double ss = block_sum(b, sred);

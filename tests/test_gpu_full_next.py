@@ -231,7 +231,9 @@ def test_union_stack_full_size():
         fin = final[g].cpu().numpy()
         mu, sd, comb = orc.zscore_max(s64)
         # The kernel's statistics: each of 256 threads sums its m = n / 256
-        # scores in fp32 (recursive summation: error <= (m - 1) 2^-24 sum |x|),
+        # scores in fp32, as four running sums of m / 4 (one per lane of a
+        # 16-byte load) added pairwise: error <= (m / 4 + 1) 2^-24 sum |x|,
+        # within the (m - 1) 2^-24 sum |x| of one running sum used below,
         # the threads' sums are added in fp64, and mu_h, then sd_h (centred
         # squares about the fp32 mean, again summed per thread in fp32, a
         # relative error <= (m + 2) 2^-24 in the variance, half that in sd_h),
