@@ -843,6 +843,12 @@ def measure_other(args, tri, synth, dev):
     torch.cuda.synchronize()
     del wk, wv, wpos, wkv
     rms, rby = [], []
+    # clocks while the rounds run (each round is one ~1.3 ms launch between
+    # host-side appends, so a clock that sags between launches shows here)
+    rclk = ClockSampler(nvsmi_gpu_id(dev.index if dev.index is not None else torch.cuda.current_device()))
+    rclk.start()
+    time.sleep(0.3)
+    rclk.mark("r0")
     for rnd in range(1, w.rounds + 1):
         kn, vn = synth.append_rows(inp, rnd, R)
         inp.k[:, :, :, B:B + R] = kn
@@ -864,10 +870,13 @@ def measure_other(args, tri, synth, dev):
         rms.append(a.elapsed_time(b))
         mv = int((keep.cpu().numpy() != np.arange(B)[None, :]).sum())
         rby.append(S * (B + R - P - W) * (d * e + 4) + mv * (4 * d * e + 8))
+    rclk.mark("r1")
+    rclk.stop()
     assert int(st.item()) == 0
     mr = sum(rms) / len(rms)
     mb = sum(rby) / len(rby)
     res["rounds"] = {"count": w.rounds, "value": S * (B + R) / (mr / 1e3), "unit": UNIT, "ms_per_round": mr,
+                     "ms_each": [round(x, 4) for x in rms], "clocks": rclk.summary("r0", "r1"),
                      "gbs": mb / mr / 1e6, "hbm_frac_of_8tbs": mb / mr / 1e6 / 8000.0,
                      "view": "capacity B + 128 rows per slice (steady state)",
                      "path": "tri_compress (one kernel: each slice scored, selected and compacted by one CTA)"}
